@@ -1,0 +1,472 @@
+#!/usr/bin/env python3
+"""Throughput benchmark: multi-scale deformable attention forward + backward.
+
+One step = msda_forward + msda_backward (all three gradients) over one batch
+of the workload, inputs already resident in HBM.  The metric is samples/s
+(samples = B*N_q*N_h*N_l*N_p) reported as Gsamples/s, plus the achieved
+fraction of the HBM roofline computed from compulsory bytes.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Default workload: the encoder shape in binary32 (B=2, N_q=L=22223, N_h=8,
+C_h=32, N_l=4, N_p=4, levels 100x167/50x84/25x42/13x21).  L2 is flushed
+(a 2x-L2 buffer is overwritten) before every timed step, outside the timed
+interval of that step.  Under torchrun each rank runs an independent replica
+on its own GPU (the operator has no cross-GPU exchange); the value is the
+samples of all ranks divided by the slowest rank's time.
+
+``--impl reference`` times the CPU oracle (float64 C loops, one thread) on a
+bounded sample of the same workload: there is no GPU implementation to
+compare against.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import platform
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from scale_deformable_attention_forward_gb300 import inputs as gen  # noqa: E402
+
+METRIC = "MSDA fwd+bwd Gsamples/s (q·h·l·p) and achieved HBM GB/s vs GB300 peak"
+UNIT = "Gsamples/s"
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCES = ["msda_kernels.cuh", "msda_launch.cuh", "msda_api.cu", "msda_forward_f32.cu",
+                  "msda_forward_bf16.cu", "msda_backward_f32.cu", "msda_backward_bf16.cu"]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")
+
+
+# ----------------------------------------------------------------------------- byte model
+def compulsory_bytes(w: gen.Workload):
+    """Compulsory HBM bytes: each tensor read or written once.
+
+    V = value, O = out / grad_output, Loc = 8 B/sample, A = 4 B/sample.
+      fwd = V + Loc + A + O
+      bwd = V + Loc + A + O + V(grad_value) + Loc(grad_loc) + A(grad_attn)
+    """
+    ev = 2 if w.dtype == "bf16" else 4
+    V = w.B * w.L * w.N_h * w.C_h * ev
+    O = w.B * w.n_queries * w.N_h * w.C_h * ev
+    S = w.samples
+    fwd = V + 8 * S + 4 * S + O
+    bwd = V + 8 * S + 4 * S + O + V + 8 * S + 4 * S
+    return fwd, bwd
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "scale_deformable_attention_forward_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch from a committed ncu capture, if it was taken on
+    the current kernel sources (else None)."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f)
+    except Exception:
+        return None
+    if rec.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return rec.get("workloads", {}).get(workload)
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", str(self.gpu_index)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+        return False
+
+    def summary(self):
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in getattr(self, "lines", []):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- distributed
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def dist_init(world, backend):
+    if world > 1:
+        import torch.distributed as dist
+        if not dist.is_initialized():
+            dist.init_process_group(backend=backend)
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """The maximum of x over all ranks (x itself without torch.distributed)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- oracle leg
+def oracle_sample(w: gen.Workload, data: dict, n_queries: int):
+    """A bounded slice of the workload for the CPU oracle: batch item 0,
+    queries [0, n_queries), every head, level and point; the full value map.
+    Arrays are widened to float64 up front (outside any timing)."""
+    n = max(1, min(n_queries, w.n_queries))
+    loc = data["sampling_locations"]
+    loc = loc[0:1, :n] if w.loc_layout == "BQHLP2" else loc[0:1, :, :n]
+    sub = {
+        "value": np.ascontiguousarray(data["value"][0:1], dtype=np.float64),
+        "sampling_locations": np.ascontiguousarray(loc, dtype=np.float64),
+        "attention_weights": np.ascontiguousarray(data["attention_weights"][0:1, :n], dtype=np.float64),
+        "grad_output": np.ascontiguousarray(data["grad_output"][0:1, :n], dtype=np.float64),
+    }
+    samples = n * w.N_h * w.N_l * w.N_p
+    return sub, samples
+
+
+def oracle_step(orc, w, data, sub):
+    kw = dict(value_layout=w.value_layout, sampling_locations_layout=w.loc_layout,
+              align_corners=w.align_corners, padding_mode=w.padding_mode)
+    orc.forward(sub["value"], data["spatial_shapes"], data["level_start_index"], sub["sampling_locations"],
+                sub["attention_weights"], **kw)
+    orc.backward(sub["grad_output"], sub["value"], data["spatial_shapes"], data["level_start_index"],
+                 sub["sampling_locations"], sub["attention_weights"], **kw)
+
+
+def cpu_model() -> str:
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu model")):
+                    return line.split(":", 1)[1].strip()
+        out = subprocess.run(["lscpu"], capture_output=True, text=True).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return platform.processor() or platform.machine()
+
+
+def time_oracle(w, data, target_s: float):
+    """Time the oracle on a slice sized for about target_s seconds."""
+    import oracle
+    orc = oracle.default()
+    probe_q = max(1, min(w.n_queries, 256))
+    sub, s = oracle_sample(w, data, probe_q)
+    t0 = time.perf_counter()
+    oracle_step(orc, w, data, sub)
+    rate = s / max(time.perf_counter() - t0, 1e-6)
+    n_q = int(min(w.n_queries, max(1, target_s * rate / (w.N_h * w.N_l * w.N_p))))
+    sub, samples = oracle_sample(w, data, n_q)
+    t0 = time.perf_counter()
+    oracle_step(orc, w, data, sub)
+    dt = time.perf_counter() - t0
+    return samples / dt / 1e9, samples, n_q, dt
+
+
+# ----------------------------------------------------------------------------- GPU leg
+def run_ours(args, w: gen.Workload):
+    import torch
+    import scale_deformable_attention_forward_gb300 as msda
+
+    world, rank, local = dist_setup()
+    torch.cuda.set_device(local)
+    dist_init(world, "nccl")
+    dev = torch.device("cuda", local)
+    msda.load_library()
+
+    data = gen.generate(w)
+    vt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    host = {
+        "value": torch.from_numpy(data["value"]).to(vt).pin_memory(),
+        "sampling_locations": torch.from_numpy(data["sampling_locations"]).pin_memory(),
+        "attention_weights": torch.from_numpy(data["attention_weights"]).pin_memory(),
+        "grad_output": torch.from_numpy(data["grad_output"]).to(vt).pin_memory(),
+    }
+    t = {k: v.to(dev) for k, v in host.items()}
+    out = torch.empty((w.B, w.n_queries, w.N_h * w.C_h), dtype=vt, device=dev)
+    gv = torch.empty_like(t["value"])
+    gl = torch.empty_like(t["sampling_locations"])
+    ga = torch.empty_like(t["attention_weights"])
+    ws_bytes = msda.msda_backward_workspace_size(t["value"], data["spatial_shapes"], data["level_start_index"],
+                                                 t["sampling_locations"], w.value_layout, w.loc_layout)
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+    kw = dict(value_layout=w.value_layout, sampling_locations_layout=w.loc_layout,
+              align_corners=w.align_corners, padding_mode=w.padding_mode)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def fwd():
+        msda.msda_forward(t["value"], data["spatial_shapes"], data["level_start_index"], t["sampling_locations"],
+                          t["attention_weights"], out=out, **kw)
+
+    def bwd():
+        msda.msda_backward(t["grad_output"], t["value"], data["spatial_shapes"], data["level_start_index"],
+                           t["sampling_locations"], t["attention_weights"], grad_value=gv,
+                           grad_sampling_locations=gl, grad_attention_weights=ga, workspace=ws, **kw)
+
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        fwd()
+        bwd()
+    torch.cuda.synchronize(dev)
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    with ClockSampler(dev.index if dev.index is not None else 0) as clk:
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        wall0 = time.perf_counter()
+        for i in range(K):
+            flush.fill_(float(i))
+            ev[i][0].record(stream)
+            fwd()
+            ev[i][1].record(stream)
+            bwd()
+            ev[i][2].record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        wall = time.perf_counter() - wall0
+    fwd_ms = [a.elapsed_time(b) for a, b, _ in ev]
+    bwd_ms = [b.elapsed_time(c) for _, b, c in ev]
+    step_ms_local = statistics.mean(f + b for f, b in zip(fwd_ms, bwd_ms))
+    step_ms = max_over_ranks(step_ms_local, world, dev)
+    value = w.samples * world / (step_ms * 1e-3) / 1e9
+
+    # End to end: pinned host inputs -> device, forward, backward, results -> pinned host.
+    host_out = {"out": torch.empty(out.shape, dtype=vt).pin_memory(),
+                "gv": torch.empty(gv.shape, dtype=vt).pin_memory(),
+                "gl": torch.empty(gl.shape, dtype=torch.float32).pin_memory(),
+                "ga": torch.empty(ga.shape, dtype=torch.float32).pin_memory()}
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = sum(v.numel() * v.element_size() for v in host_out.values())
+    K_e2e = max(3, min(K, 200))
+
+    def e2e_step():
+        for k in host:
+            t[k].copy_(host[k], non_blocking=True)
+        fwd()
+        bwd()
+        host_out["out"].copy_(out, non_blocking=True)
+        host_out["gv"].copy_(gv, non_blocking=True)
+        host_out["gl"].copy_(gl, non_blocking=True)
+        host_out["ga"].copy_(ga, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(K_e2e):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / K_e2e, world, dev)
+    barrier(world)
+
+    fwd_b, bwd_b = compulsory_bytes(w)
+    peak, peak_kind = measured_peaks()
+    fwd_mean, bwd_mean = statistics.mean(fwd_ms), statistics.mean(bwd_ms)
+    dominant = "msda_backward" if bwd_mean >= fwd_mean else "msda_forward"
+    dom_bytes, dom_ms = (bwd_b, bwd_mean) if dominant == "msda_backward" else (fwd_b, fwd_mean)
+    achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
+    traffic = recorded_traffic(args.workload)
+    launches_per_step = 1 + 2 + (1 if w.dtype == "bf16" else 0)  # fwd; zero-fill + bwd; bf16 finalise
+
+    result = {
+        "metric": METRIC,
+        "value": round(value, 4),
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(step_ms, 6),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32" if w.dtype == "f32" else "bf16 storage, f32 arithmetic",
+        "data": "synthetic (seeded Deformable-DETR-shaped inputs)",
+        "config": {"workload": gen.WORKLOAD_DESCRIPTIONS.get(args.workload, args.workload),
+                   "name": args.workload, "samples_per_step_per_gpu": w.samples,
+                   "l2": "flushed before every step (2x L2 buffer overwritten, outside the timed interval)",
+                   "parallelism": f"replicas x{world} (no cross-GPU exchange)"},
+        "fwd_ms": round(fwd_mean, 6),
+        "bwd_ms": round(bwd_mean, 6),
+        "wall_s_timed_region": round(wall, 3),
+        "clocks": clk.summary(),
+        "e2e": {"value": round(w.samples * world / (e2e_ms * 1e-3) / 1e9, 4), "unit": UNIT,
+                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "path": "pinned host -> device copies, msda_forward, msda_backward, device -> pinned host"},
+        "gpu_launches": launches_per_step * K,
+        "roofline": {
+            "kernel": dominant + (" (zero-fill + fused gather/scatter kernel)" if dominant == "msda_backward"
+                                  else " (gather kernel)"),
+            "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(achieved / peak, 4), "peak_source": f"{peak_kind} hbm_gbs",
+            "algorithmic_bytes_per_launch": dom_bytes,
+            "traffic": (traffic or {}).get(dominant),
+        },
+        "roofline_step": {
+            "what": "forward + backward compulsory bytes / step time",
+            "achieved": round((fwd_b + bwd_b) / (step_ms * 1e-3) / 1e9, 1), "peak": peak, "unit": "GB/s",
+            "frac": round((fwd_b + bwd_b) / (step_ms * 1e-3) / 1e9 / peak, 4),
+            "bytes_per_step": fwd_b + bwd_b,
+        },
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, samples, n_q, dt = time_oracle(w, data, args.cpu_seconds)
+        result["cpu_baseline"] = {
+            "value": round(v, 6), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"batch item 0, queries [0,{n_q}) of {w.n_queries}, all heads/levels/points "
+                      f"({samples} samples), forward + backward once, float64, {dt:.1f} s",
+            "cpu": cpu_model()}
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_reference(args, w: gen.Workload):
+    """The oracle on the host cores, on a bounded slice per step."""
+    world, rank, _ = dist_setup()
+    if rank != 0:
+        return
+    import oracle
+    orc = oracle.default()
+    data = gen.generate(w)
+    total_steps = args.warmup + args.steps
+    per_step_s = max(0.005, args.reference_seconds / max(1, total_steps))
+    probe_q = max(1, min(w.n_queries, 64))
+    sub, s = oracle_sample(w, data, probe_q)
+    t0 = time.perf_counter()
+    oracle_step(orc, w, data, sub)
+    rate = s / max(time.perf_counter() - t0, 1e-6)
+    n_q = int(min(w.n_queries, max(1, per_step_s * rate / (w.N_h * w.N_l * w.N_p))))
+    sub, samples = oracle_sample(w, data, n_q)
+    for _ in range(args.warmup):
+        oracle_step(orc, w, data, sub)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(orc, w, data, sub)
+    dt = time.perf_counter() - t0
+    value = samples * args.steps / dt / 1e9
+    result = {
+        "impl": "reference",
+        "metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded Deformable-DETR-shaped inputs)",
+        "config": {"workload": gen.WORKLOAD_DESCRIPTIONS.get(args.workload, args.workload), "name": args.workload},
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "kind": "oracle", "cores": 1,
+                         "sample": f"per step: batch item 0, queries [0,{n_q}) of {w.n_queries}, all "
+                                   f"heads/levels/points ({samples} samples), forward + backward, float64",
+                         "cpu": cpu_model()},
+        "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "note": "no GPU implementation exists for this operator on the reference pages; the reference arm "
+                "is the float64 CPU oracle",
+    }
+    print(json.dumps(result), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default="encoder32", choices=sorted(gen.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
+                    help="CPU work for the cpu_baseline leg (a slice of the workload)")
+    ap.add_argument("--reference-seconds", type=float, default=90.0,
+                    help="total CPU time budget of --impl reference (split over warm-up + steps)")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    w = gen.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,177 @@
+/*
+ * msda.h -- C ABI of libmsda: multi-scale deformable attention (MSDA),
+ * forward and backward, on an NVIDIA GB300 (sm_103a).
+ *
+ * The operations follow two pages of the AWS Neuron NKI library:
+ *   "MS Deformable Attention Kernel API Reference" (the forward:
+ *    Background, Parameters, Returns) and
+ *   "MS Deformable Attention Backward Kernel API Reference" (the backward:
+ *    Background, Parameters, Returns, Notes).
+ *
+ * Definitions used by every entry point.  A sample s = (b, q, h, l, p) has a
+ * normalised location (x, y) and an attention weight A_s.  Its pixel
+ * coordinate on level l (H_l rows, W_l columns) is
+ *     align_corners = 0:  px = x * W_l - 0.5,   py = y * H_l - 0.5
+ *     align_corners = 1:  px = x * (W_l - 1),   py = y * (H_l - 1)
+ * (forward page, Parameters: align_corners).  The sample S_s is the bilinear
+ * interpolation of the head-h value map of level l at (px, py), over the four
+ * corners of the cell floor(px), floor(py).  With padding "zeros" a corner
+ * outside the map reads 0; with "border" each corner index is clamped into
+ * the map (Parameters: padding_mode; backward page, Notes).  Pixel (y, x) of
+ * level l is row level_start_index[l] + y * W_l + x of the flattened L axis.
+ *     out[b, q, h*C_h + c] = sum_l sum_p A_s * S_s[c]      (forward, Returns)
+ * The backward returns the derivatives of <grad_output, out> with respect to
+ * value, sampling_locations and attention_weights (backward page, Background
+ * and Returns).
+ *
+ * Memory and threading rules for every call:
+ *   - All tensor pointers are DEVICE pointers, C-contiguous in the layout the
+ *     descriptor names, owned by the caller.  The library allocates nothing,
+ *     keeps no pointer after the call returns and never synchronises.
+ *   - spatial_shapes and level_start_index are HOST arrays read during the
+ *     call only.
+ *   - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL is
+ *     the legacy default stream) on the current device.  Results are ready
+ *     when the stream reaches that point.
+ *   - Every argument is validated before anything is enqueued: a call that
+ *     returns an error has not touched any output.
+ *   - Functions are thread-safe; concurrent calls on different streams may
+ *     not share output buffers.
+ */
+#ifndef MSDA_H
+#define MSDA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* The CUDA runtime's stream handle (same declaration as in driver_types.h). */
+typedef struct CUstream_st *cudaStream_t;
+
+/* Layout of `value` and of `grad_value` (forward page, Parameters: value,
+ * value_layout).  Default BLNC. */
+enum msda_value_layout {
+    MSDA_LAYOUT_BLNC = 0, /* (B, L, N_h, C_h) */
+    MSDA_LAYOUT_BNLC = 1  /* (B, N_h, L, C_h) */
+};
+
+/* Layout of `sampling_locations` and its gradient (forward page, Parameters:
+ * sampling_locations, sampling_locations_layout).  The "2" axis holds (x, y):
+ * x runs along the width W_l, y along the height H_l.  Default BQHLP2. */
+enum msda_loc_layout {
+    MSDA_LAYOUT_BQHLP2 = 0, /* (B, N_q, N_h, N_l, N_p, 2) */
+    MSDA_LAYOUT_B2QHLP = 1  /* (B, 2, N_q, N_h, N_l, N_p) */
+};
+
+/* padding_mode (forward page, Parameters; backward page, Notes). */
+enum msda_padding {
+    MSDA_PADDING_ZEROS = 0, /* a bilinear corner outside the map reads 0 */
+    MSDA_PADDING_BORDER = 1 /* a bilinear corner is clamped onto the edge */
+};
+
+/* Element types. */
+enum msda_dtype {
+    MSDA_DTYPE_F32 = 0, /* IEEE binary32 */
+    MSDA_DTYPE_BF16 = 1 /* bfloat16; arithmetic is binary32, stores round to nearest even */
+};
+
+/* Status codes: 0 on success, negative on failure. */
+enum msda_status {
+    MSDA_OK = 0,
+    MSDA_ERR_NULL_POINTER = -1, /* a tensor with elements, the descriptor or a level array is NULL */
+    MSDA_ERR_BAD_ENUM = -2,     /* layout / padding / dtype / flag value out of range */
+    MSDA_ERR_BAD_DIM = -3,      /* a dimension is negative, or N_l > MSDA_MAX_LEVELS */
+    MSDA_ERR_NO_OUTPUT = -4,    /* backward with all three compute_grad_* flags 0 */
+    MSDA_ERR_LEVELS = -5,       /* H_l or W_l < 1, level_start_index[0] != 0,
+                                   start[l+1] != start[l] + H_l*W_l, or L != sum H_l*W_l */
+    MSDA_ERR_WORKSPACE = -6,    /* workspace smaller than msda_backward_workspace_size() */
+    MSDA_ERR_TOO_LARGE = -7,    /* a size exceeds the 32-bit index limits stated below */
+    MSDA_ERR_UNSUPPORTED = -8,  /* a valid but unimplemented combination (loc_dtype BF16,
+                                   C_h > 256 with unaligned pointers) */
+    MSDA_ERR_MISALIGNED = -9,   /* a pointer not aligned to its element size */
+    MSDA_ERR_CUDA = -10         /* the CUDA runtime reported an error (msda_last_cuda_error) */
+};
+
+/* Levels the descriptor may describe. */
+#define MSDA_MAX_LEVELS 16
+
+/* Problem descriptor.  Dimensions follow the pages' Dimensions list:
+ *   B batch, N_q queries, N_h heads, C_h channels per head, N_l levels,
+ *   N_p points per query, head and level, L = sum_l H_l * W_l.
+ * Zero-sized dimensions are allowed (empty tensors).  Index limits:
+ *   L * N_h * C_h, N_q * N_h * N_l * N_p * 2 and B * N_q * N_h must each be
+ *   below 2^31. */
+typedef struct msda_desc {
+    int64_t B, N_q, N_h, C_h, N_l, N_p, L;
+    const int64_t *spatial_shapes;    /* host, N_l pairs (H_l, W_l) */
+    const int64_t *level_start_index; /* host, N_l entries; start of level l in L */
+    int32_t value_layout;             /* enum msda_value_layout */
+    int32_t loc_layout;               /* enum msda_loc_layout */
+    int32_t align_corners;            /* 0 or 1 (default 0) */
+    int32_t padding_mode;             /* enum msda_padding */
+    int32_t value_dtype;              /* enum msda_dtype of value, out, grad_output, grad_value */
+    int32_t loc_dtype;                /* enum msda_dtype of sampling_locations,
+                                         attention_weights and their gradients
+                                         (only MSDA_DTYPE_F32 is implemented) */
+} msda_desc;
+
+/* Forward ("MS Deformable Attention Kernel API Reference", Parameters and
+ * Returns).
+ *   value               (B,L,N_h,C_h) or (B,N_h,L,C_h), value_dtype
+ *   sampling_locations  (B,N_q,N_h,N_l,N_p,2) or (B,2,N_q,N_h,N_l,N_p), loc_dtype
+ *   attention_weights   (B,N_q,N_h,N_l,N_p), loc_dtype
+ *   out                 (B,N_q,N_h*C_h), value_dtype, column h*C_h + c;
+ *                       fully overwritten.
+ * Returns MSDA_OK or a negative msda_status. */
+int msda_forward(const msda_desc *desc, const void *value, const void *sampling_locations,
+                 const void *attention_weights, void *out, cudaStream_t stream);
+
+/* Bytes of device workspace msda_backward needs: B*L*N_h*C_h*4 (a binary32
+ * accumulator for grad_value) when compute_grad_value is set and value_dtype
+ * is BF16, else 0.  Returns 0 for an invalid descriptor. */
+size_t msda_backward_workspace_size(const msda_desc *desc, int compute_grad_value);
+
+/* Backward ("MS Deformable Attention Backward Kernel API Reference",
+ * Parameters and Returns; gradients are the bilinear-interpolation
+ * derivatives, Notes).
+ *   grad_output         (B,N_q,N_h*C_h), value_dtype
+ *   value               as in msda_forward; may be NULL when only
+ *                       compute_grad_value is set (it is not read then)
+ *   sampling_locations  as in msda_forward
+ *   attention_weights   as in msda_forward; may be NULL when only
+ *                       compute_grad_attention_weights is set
+ *   compute_grad_*      0 or 1 each, at least one 1 (Parameters:
+ *                       compute_grad_value / _sampling_locations /
+ *                       _attention_weights)
+ *   grad_value          value's shape, layout and dtype; overwritten
+ *   grad_sampling_locations  sampling_locations' shape and layout, binary32
+ *   grad_attention_weights   (B,N_q,N_h,N_l,N_p), binary32
+ *   A disabled output is neither read nor written and may be NULL.
+ *   workspace           device scratch of at least
+ *                       msda_backward_workspace_size(desc, compute_grad_value)
+ *                       bytes (NULL when that is 0), 16-byte aligned; its
+ *                       contents on entry do not matter.
+ * grad_value is accumulated with binary32 atomics, so its summation order
+ * (and last-bit rounding) varies from run to run.
+ * Returns MSDA_OK or a negative msda_status. */
+int msda_backward(const msda_desc *desc, const void *grad_output, const void *value,
+                  const void *sampling_locations, const void *attention_weights,
+                  int compute_grad_value, int compute_grad_sampling_locations,
+                  int compute_grad_attention_weights, void *grad_value,
+                  void *grad_sampling_locations, void *grad_attention_weights, void *workspace,
+                  size_t workspace_bytes, cudaStream_t stream);
+
+/* A static, human-readable description of a status code. */
+const char *msda_status_string(int status);
+
+/* The cudaError_t behind the calling thread's last MSDA_ERR_CUDA (0 if none). */
+int msda_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MSDA_H */

@@ -1,0 +1,8 @@
+// Backward kernels for f32 value tensors.
+#include "msda_launch.cuh"
+
+namespace msda {
+template cudaError_t launch_backward<float>(const Params &, bool, int, int, const float *, const float *,
+                                          const float *, const float *, float *, float *, float *, int,
+                                          cudaStream_t);
+}  // namespace msda

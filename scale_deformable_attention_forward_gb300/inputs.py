@@ -226,9 +226,12 @@ def generate(w: Workload, seed: Optional[int] = None) -> dict:
         raise ValueError(f"unknown location recipe {w.loc_recipe!r}")
 
     logits = rng.standard_normal((B, Nq, Nh, Nl * Np))
-    logits -= logits.max(axis=-1, keepdims=True)
-    e = np.exp(logits)
-    attn = (e / e.sum(axis=-1, keepdims=True)).reshape(B, Nq, Nh, Nl, Np)
+    if logits.size:
+        logits -= logits.max(axis=-1, keepdims=True)
+        e = np.exp(logits)
+        attn = (e / e.sum(axis=-1, keepdims=True)).reshape(B, Nq, Nh, Nl, Np)
+    else:
+        attn = np.zeros((B, Nq, Nh, Nl, Np))
 
     grad_output = rng.standard_normal((B, Nq, Nh * Ch))
 

@@ -1,0 +1,130 @@
+"""The C-ABI library on the CPU: it loads, exports every symbol include/*.h
+declares, and rejects invalid arguments before any CUDA call (no GPU is
+touched by these tests)."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+import scale_deformable_attention_forward_gb300 as msda
+from scale_deformable_attention_forward_gb300 import build as msda_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    msda_build.build()
+    return msda.load_library()
+
+
+def _declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        for m in re.finditer(r"\b([a-z_][a-z0-9_]*)\s*\([^;{]*\)\s*;", text):
+            names.add(m.group(1))
+    return names
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _declared_functions()
+    assert {"msda_forward", "msda_backward", "msda_backward_workspace_size", "msda_status_string",
+            "msda_last_cuda_error"} <= names
+    for n in sorted(names):
+        assert hasattr(lib, n), f"{n} declared in include/ but not exported"
+
+
+def test_status_strings(lib):
+    for code in range(-10, 1):
+        s = msda.msda_status_string(code)
+        assert s and s != "unknown status"
+    assert msda.msda_status_string(-99) == "unknown status"
+    assert lib.msda_last_cuda_error() == 0
+
+
+LEVELS = ((4, 6), (2, 3))
+STARTS = (0, 24)
+DIMS = (2, 5, 3, 8, 2, 4, 30)  # B, N_q, N_h, C_h, N_l, N_p, L
+FAKE = ctypes.c_void_p(0x10000)  # never dereferenced: every case below fails validation
+
+# The rejection tests hand the library placeholder pointers.  They are meant
+# to fail validation before any launch; to rule out a launch on a placeholder
+# should validation ever regress, they run only where no GPU is visible.
+no_gpu = pytest.mark.skipif(
+    __import__("torch").cuda.is_available(), reason="placeholder-pointer tests run only without a GPU")
+
+
+def _fwd(lib, desc, value=FAKE, loc=FAKE, attn=FAKE, out=FAKE):
+    return lib.msda_forward(desc.ref() if desc is not None else None, value, loc, attn, out, None)
+
+
+def _bwd(lib, desc, flags=(1, 1, 1), ws=None, ws_bytes=0, **ptrs):
+    p = dict(go=FAKE, value=FAKE, loc=FAKE, attn=FAKE, gv=FAKE, gl=FAKE, ga=FAKE)
+    p.update(ptrs)
+    return lib.msda_backward(desc.ref(), p["go"], p["value"], p["loc"], p["attn"], *flags, p["gv"], p["gl"],
+                             p["ga"], ws, ws_bytes, None)
+
+
+@no_gpu
+def test_rejections_forward(lib):
+    d = msda.make_desc
+    assert _fwd(lib, None) == -1
+    assert _fwd(lib, d(DIMS, LEVELS, STARTS), out=None) == -1
+    assert _fwd(lib, d(DIMS, LEVELS, STARTS), value=None) == -1
+    bad = d(DIMS, LEVELS, STARTS)
+    bad.c.value_layout = 7
+    assert _fwd(lib, bad) == -2
+    bad = d(DIMS, LEVELS, STARTS)
+    bad.c.padding_mode = 2
+    assert _fwd(lib, bad) == -2
+    bad = d(DIMS, LEVELS, STARTS)
+    bad.c.align_corners = 3
+    assert _fwd(lib, bad) == -2
+    assert _fwd(lib, d((2, -1, 3, 8, 2, 4, 30), LEVELS, STARTS)) == -3
+    assert _fwd(lib, d((2, 5, 3, 8, 17, 4, 30), LEVELS * 9, STARTS * 9)) == -3
+    assert _fwd(lib, d(DIMS, LEVELS, (1, 24))) == -5          # start[0] != 0
+    assert _fwd(lib, d(DIMS, LEVELS, (0, 23))) == -5          # start[1] != H0*W0
+    assert _fwd(lib, d((2, 5, 3, 8, 2, 4, 31), LEVELS, STARTS)) == -5  # L != sum
+    assert _fwd(lib, d(DIMS, ((0, 6), (2, 3)), (0, 0))) == -5  # empty level
+    assert _fwd(lib, d(DIMS, LEVELS, STARTS, value_dtype=msda.DTYPE_F32, loc_dtype=1)) == -8
+    assert _fwd(lib, d(DIMS, LEVELS, STARTS), value=ctypes.c_void_p(0x10002)) == -9
+    big = ((46341, 46341),)
+    assert _fwd(lib, d((1, 1, 1, 1, 1, 1, 46341 * 46341), big, (0,))) == -7
+    assert _fwd(lib, d((1, 1, 64, 64, 1, 1, 1 << 20), ((1024, 1024),), (0,))) == -7
+
+
+@no_gpu
+def test_rejections_backward(lib):
+    d = msda.make_desc(DIMS, LEVELS, STARTS)
+    assert _bwd(lib, d, flags=(0, 0, 0)) == -4
+    assert _bwd(lib, d, flags=(2, 0, 0)) == -2
+    assert _bwd(lib, d, gv=None) == -1
+    assert _bwd(lib, d, flags=(0, 1, 0), gl=None) == -1
+    assert _bwd(lib, d, flags=(0, 0, 1), ga=None) == -1
+    assert _bwd(lib, d, flags=(0, 1, 0), value=None) == -1
+    assert _bwd(lib, d, flags=(1, 0, 0), attn=None) == -1     # grad_value needs the weights
+    assert _bwd(lib, d, flags=(1, 0, 0), gv=ctypes.c_void_p(0x10001)) == -9
+    bf = msda.make_desc(DIMS, LEVELS, STARTS, value_dtype=msda.DTYPE_BF16)
+    need = lib.msda_backward_workspace_size(bf.ref(), 1)
+    assert need == 2 * 30 * 3 * 8 * 4
+    assert lib.msda_backward_workspace_size(bf.ref(), 0) == 0
+    assert lib.msda_backward_workspace_size(d.ref(), 1) == 0
+    assert _bwd(lib, bf, ws=None, ws_bytes=0) == -6
+    assert _bwd(lib, bf, ws=FAKE, ws_bytes=need - 1) == -6
+    assert _bwd(lib, bf, ws=None, ws_bytes=need) == -1
+    assert _bwd(lib, bf, ws=ctypes.c_void_p(0x10004), ws_bytes=need) == -9
+
+
+def test_python_binding_rejects_cpu_tensors(lib):
+    torch = pytest.importorskip("torch")
+    v = torch.zeros(1, 30, 1, 4)
+    loc = torch.zeros(1, 2, 1, 2, 1, 2)
+    a = torch.zeros(1, 2, 1, 2, 1)
+    with pytest.raises(ValueError):
+        msda.msda_forward(v, LEVELS, STARTS, loc, a)
+    with pytest.raises(ValueError):
+        msda.msda_backward(torch.zeros(1, 2, 4), v, LEVELS, STARTS, loc, a)

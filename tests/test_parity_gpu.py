@@ -1,0 +1,235 @@
+"""GPU parity: the sm_103a kernels (through the Python binding and the C ABI)
+against the float64 CPU oracle, element by element, on seeded inputs.
+
+Covers the five Deformable-DETR-shaped workloads at full size, the layout x
+padding x align_corners x dtype matrix on a multi-tile problem with ragged
+tails, every compute_grad_* combination, channel counts that exercise every
+kernel shape (vector and scalar paths, masked lanes), unaligned pointers,
+degenerate levels, extreme and exactly-on-grid locations, and empty inputs.
+"""
+import numpy as np
+import pytest
+
+from parity_util import (RTOL, assert_close, check_workload, gpu_backward, gpu_forward, np64, oracle_backward,
+                         oracle_forward, to_device)
+from scale_deformable_attention_forward_gb300 import inputs as gen
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+ALL_FLAGS = [(True, True, True), (True, False, False), (False, True, False), (False, False, True),
+             (True, True, False), (False, True, True), (True, False, True)]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from scale_deformable_attention_forward_gb300 import build
+    build.build()
+
+
+# ------------------------------------------------------------------ full-size workloads
+@pytest.mark.parametrize("name", ["tiny", "decoder", "encoder32", "encoder16", "hires16"])
+def test_workload_full_size(name):
+    w = gen.WORKLOADS[name]
+    flag_sets = [(True, True, True)]
+    if name == "hires16":
+        flag_sets += [(True, False, False), (False, True, True)]
+    if name == "tiny":
+        flag_sets = ALL_FLAGS
+    check_workload(w, flag_sets=flag_sets)
+
+
+# ------------------------------------------------------------------ option matrix
+MATRIX_LEVELS = ((13, 17), (7, 9), (3, 4), (1, 1))
+
+
+def _small(dtype, vl, ll, align, pad, C_h=32, N_q=37, N_p=3, B=2, N_h=3, levels=MATRIX_LEVELS, seed=11,
+           lo=-0.15, hi=1.15):
+    return gen.Workload(f"m-{dtype}-{vl}-{ll}-{align}-{pad}-C{C_h}", B=B, N_q=N_q, N_h=N_h, C_h=C_h, N_p=N_p,
+                        levels=levels, dtype=dtype, value_layout=vl, loc_layout=ll, align_corners=align,
+                        padding_mode=pad, loc_recipe="uniform", loc_lo=lo, loc_hi=hi, seed=seed)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("vl", ["BLNC", "BNLC"])
+@pytest.mark.parametrize("ll", ["BQHLP2", "B2QHLP"])
+@pytest.mark.parametrize("align", [False, True])
+@pytest.mark.parametrize("pad", ["zeros", "border"])
+def test_option_matrix(dtype, vl, ll, align, pad):
+    check_workload(_small(dtype, vl, ll, align, pad), flag_sets=[(True, True, True), (False, True, True)])
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("C_h", [1, 3, 4, 5, 8, 12, 16, 24, 40, 64, 96, 200, 256])
+def test_channel_counts(dtype, C_h):
+    """Every (vector width, lanes per sample, chunks per lane) instantiation,
+    including masked lanes and the scalar fallback."""
+    w = _small(dtype, "BLNC", "BQHLP2", False, "zeros", C_h=C_h, N_q=9, N_h=2, N_p=2, seed=C_h)
+    check_workload(w, flag_sets=[(True, True, True)])
+
+
+@pytest.mark.parametrize("N_p", [1, 5, 8, 13])
+def test_points_per_level(N_p):
+    """N_l*N_p not a multiple of the samples in flight per warp."""
+    check_workload(_small("f32", "BLNC", "BQHLP2", False, "zeros", N_p=N_p, N_q=11, seed=50 + N_p),
+                   flag_sets=ALL_FLAGS[:4])
+
+
+def test_many_levels():
+    levels = tuple((3 + i, 2 + (i * 5) % 7) for i in range(16))
+    check_workload(_small("f32", "BNLC", "B2QHLP", True, "border", levels=levels, N_q=7, N_p=2, seed=61))
+
+
+# ------------------------------------------------------------------ flags and untouched outputs
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_disabled_outputs_untouched(dtype):
+    w = _small(dtype, "BLNC", "BQHLP2", False, "zeros", seed=71)
+    d = gen.generate(w)
+    t = to_device(d, w.dtype)
+    for flags in ALL_FLAGS:
+        sentinels = {
+            "grad_value": torch.full_like(t["value"], 7.0),
+            "grad_sampling_locations": torch.full_like(t["sampling_locations"], 7.0),
+            "grad_attention_weights": torch.full_like(t["attention_weights"], 7.0),
+        }
+        import scale_deformable_attention_forward_gb300 as msda
+        lib = msda.load_library()
+        desc = msda.make_desc((w.B, w.n_queries, w.N_h, w.C_h, w.N_l, w.N_p, w.L), d["spatial_shapes"],
+                              d["level_start_index"], w.value_layout, w.loc_layout, w.align_corners,
+                              w.padding_mode, msda.DTYPE_BF16 if dtype == "bf16" else msda.DTYPE_F32)
+        ws_n = lib.msda_backward_workspace_size(desc.ref(), int(flags[0]))
+        ws = torch.empty(max(ws_n, 16), dtype=torch.uint8, device="cuda")
+        P = lambda x: x.data_ptr()
+        rc = lib.msda_backward(desc.ref(), P(t["grad_output"]), P(t["value"]), P(t["sampling_locations"]),
+                               P(t["attention_weights"]), *[int(f) for f in flags],
+                               P(sentinels["grad_value"]), P(sentinels["grad_sampling_locations"]),
+                               P(sentinels["grad_attention_weights"]), P(ws), ws_n,
+                               torch.cuda.current_stream().cuda_stream)
+        assert rc == 0
+        torch.cuda.synchronize()
+        ref = oracle_backward(w, d, flags)
+        for (name, buf), f, r in zip(sentinels.items(), flags, ref):
+            if f:
+                assert_close(np64(buf), r, RTOL[(dtype, "bwd")], f"{name} {flags}")
+            else:
+                assert torch.all(buf == 7.0), f"{name} written although disabled ({flags})"
+
+
+# ------------------------------------------------------------------ special locations
+def _custom(levels, loc, value=None, attn=None, g=None, N_h=2, C_h=8, dtype="f32", **opt):
+    B, N_q = loc.shape[0], loc.shape[1]
+    N_p = loc.shape[4]
+    rng = np.random.default_rng(5)
+    L = sum(h * w for h, w in levels)
+    w = gen.Workload("custom", B=B, N_q=N_q, N_h=N_h, C_h=C_h, N_p=N_p, levels=levels, dtype=dtype, **opt)
+    d = {
+        "value": gen.to_value_layout(gen.store_dtype(rng.standard_normal((B, L, N_h, C_h)) if value is None
+                                                     else value, dtype), w.value_layout),
+        "sampling_locations": gen.to_loc_layout(np.asarray(loc, dtype=np.float32), w.loc_layout),
+        "attention_weights": np.asarray(rng.uniform(0.1, 1.0, (B, N_q, N_h, len(levels), N_p))
+                                        if attn is None else attn, dtype=np.float32),
+        "grad_output": gen.store_dtype(rng.standard_normal((B, N_q, N_h * C_h)) if g is None else g, dtype),
+        "spatial_shapes": levels,
+        "level_start_index": w.level_start_index,
+    }
+    return w, d
+
+
+@pytest.mark.parametrize("pad", ["zeros", "border"])
+@pytest.mark.parametrize("align", [False, True])
+def test_extreme_and_on_grid_locations(pad, align):
+    levels = ((5, 7), (3, 2), (1, 4))
+    specials = [-1e30, -1e6, -5.0, -1.0, -0.5, -1e-7, 0.0, 1e-7, 0.25, 0.5, 1.0 - 1e-7, 1.0, 1.0 + 1e-7, 1.5,
+                5.0, 1e6, 1e30]
+    # integer pixel coordinates and pixel centres of every level, in both mappings
+    for H, W in levels:
+        for n in (H, W):
+            specials += [k / n for k in range(n + 1)] + [(k + 0.5) / n for k in range(n)]
+            if n > 1:
+                specials += [k / (n - 1) for k in range(n)]
+    sp = np.array(specials, dtype=np.float32)
+    rng = np.random.default_rng(9)
+    N_q, N_p = 40, 4
+    loc = rng.choice(sp, size=(2, N_q, 2, len(levels), N_p, 2))
+    w, d = _custom(levels, loc, padding_mode=pad, align_corners=align)
+    check_workload(w, d=d, flag_sets=[(True, True, True)])
+
+
+def test_single_pixel_and_single_row_levels_align_corners():
+    """W_l = 1 or H_l = 1 with align_corners=True: that axis always maps to 0
+    and its location gradient is 0."""
+    levels = ((1, 1), (1, 6), (5, 1))
+    rng = np.random.default_rng(10)
+    loc = rng.uniform(-0.2, 1.2, size=(1, 16, 2, 3, 3, 2))
+    for pad in ("zeros", "border"):
+        w, d = _custom(levels, loc, padding_mode=pad, align_corners=True)
+        check_workload(w, d=d, flag_sets=ALL_FLAGS[:1])
+
+
+# ------------------------------------------------------------------ pointers, streams, empties
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_unaligned_pointers_take_scalar_path(dtype):
+    """Tensors that start one element past a 16-byte boundary are still
+    accepted (element-aligned) and give the same results."""
+    w = _small(dtype, "BLNC", "BQHLP2", False, "zeros", C_h=32, N_q=13, seed=81)
+    d = gen.generate(w)
+    t = to_device(d, w.dtype)
+    shifted = {}
+    for k, v in t.items():
+        buf = torch.empty(v.numel() + 1, dtype=v.dtype, device=v.device)
+        s = buf[1:].view(v.shape)
+        s.copy_(v)
+        shifted[k] = s
+    out = gpu_forward(w, shifted, d)
+    gv_buf = torch.empty(t["value"].numel() + 1, dtype=t["value"].dtype, device="cuda")
+    got = gpu_backward(w, shifted, d, grad_value=gv_buf[1:].view(t["value"].shape))
+    torch.cuda.synchronize()
+    assert_close(np64(out), oracle_forward(w, d), RTOL[(dtype, "fwd")], "unaligned out")
+    for g, r, n in zip(got, oracle_backward(w, d), ("gv", "gl", "ga")):
+        assert_close(np64(g), r, RTOL[(dtype, "bwd")], f"unaligned {n}")
+
+
+def test_non_default_stream():
+    w = _small("f32", "BLNC", "BQHLP2", False, "zeros", seed=91)
+    d = gen.generate(w)
+    t = to_device(d, w.dtype)
+    s = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        out = gpu_forward(w, t, d)
+        got = gpu_backward(w, t, d)
+    s.synchronize()
+    assert_close(np64(out), oracle_forward(w, d), RTOL[("f32", "fwd")], "stream out")
+    assert_close(np64(got[0]), oracle_backward(w, d)[0], RTOL[("f32", "bwd")], "stream gv")
+
+
+@pytest.mark.parametrize("dims", [dict(B=0), dict(N_q=0), dict(N_p=0), dict(C_h=0), dict(N_h=0)])
+def test_empty_inputs(dims):
+    base = dict(B=2, N_q=5, N_h=2, C_h=8, N_p=2)
+    base.update(dims)
+    w = gen.Workload("empty", levels=((4, 5), (2, 2)), loc_recipe="uniform", seed=3, **base)
+    d = gen.generate(w)
+    t = to_device(d, w.dtype)
+    out = gpu_forward(w, t, d)
+    got = gpu_backward(w, t, d)
+    torch.cuda.synchronize()
+    assert_close(np64(out), oracle_forward(w, d), 1e-5, "empty out")
+    for g, r in zip(got, oracle_backward(w, d)):
+        assert_close(np64(g), r, 1e-4, "empty grads")
+
+
+def test_repeatable():
+    """The forward and the location/attention gradients are bit-identical
+    from run to run (no atomics there); grad_value stays within tolerance."""
+    w = gen.WORKLOADS["decoder"]
+    d = gen.generate(w)
+    t = to_device(d, w.dtype)
+    o1, o2 = gpu_forward(w, t, d).clone(), gpu_forward(w, t, d).clone()
+    a = [x.clone() for x in gpu_backward(w, t, d)]
+    b = [x.clone() for x in gpu_backward(w, t, d)]
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2)
+    assert torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])
+    assert_close(np64(a[0]), np64(b[0]), 1e-5, "grad_value run to run")
