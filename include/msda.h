@@ -164,6 +164,41 @@ int msda_backward(const msda_desc *desc, const void *grad_output, const void *va
                   void *grad_sampling_locations, void *grad_attention_weights, void *workspace,
                   size_t workspace_bytes, cudaStream_t stream);
 
+/* Size of the library-owned scratch array used by msda_backward_noalloc:
+ * 32 MiB, i.e. room for a binary32 accumulator of B*L*N_h*C_h <= 8,388,608
+ * elements (one 4-level Deformable-DETR pyramid image with 8 heads of 32
+ * channels needs 5,689,088). */
+#define MSDA_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+
+/* msda_backward for callers that cannot allocate device memory.  The pages
+ * have no counterpart: it exists for hosts that may not call cudaMalloc (a
+ * plug-in living inside another application's memory pool, a loop where
+ * allocation is forbidden after start-up, a caller that can only hand over
+ * the tensors it already owns).
+ *
+ * Arguments and results are those of msda_backward without the workspace:
+ * the binary32 grad_value accumulator that bfloat16 value needs lives in a
+ * fixed array inside the library (MSDA_NOALLOC_SCRATCH_BYTES, held on every
+ * GPU that loads the library until the process exits).  A problem whose
+ * accumulator would not fit (bfloat16 value, compute_grad_value set and
+ * B*L*N_h*C_h*4 > MSDA_NOALLOC_SCRATCH_BYTES) is refused with
+ * MSDA_ERR_WORKSPACE before anything is enqueued; binary32 value needs no
+ * scratch and has no such limit.  Nothing is allocated.
+ *
+ * The first call on a device looks up the array's device address on that
+ * (current) device; make that first call before any stream capture.  All
+ * calls share the one array, which keeps the last call's contents (each call
+ * clears what it uses): calls whose GPU work overlaps -- different streams,
+ * or unordered host threads -- race on it and corrupt grad_value.  Returns
+ * MSDA_OK or a negative msda_status (MSDA_ERR_CUDA also when the address
+ * lookup fails). */
+int msda_backward_noalloc(const msda_desc *desc, const void *grad_output, const void *value,
+                          const void *sampling_locations, const void *attention_weights,
+                          int compute_grad_value, int compute_grad_sampling_locations,
+                          int compute_grad_attention_weights, void *grad_value,
+                          void *grad_sampling_locations, void *grad_attention_weights,
+                          cudaStream_t stream);
+
 /* A static, human-readable description of a status code. */
 const char *msda_status_string(int status);
 

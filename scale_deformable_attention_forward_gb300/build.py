@@ -21,7 +21,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libmsda.so")
 
 SOURCES = ["msda_api.cu", "msda_forward_f32.cu", "msda_forward_bf16.cu", "msda_backward_f32.cu",
-           "msda_backward_bf16.cu"]
+           "msda_backward_bf16.cu", "msda_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
 
