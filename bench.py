@@ -42,8 +42,7 @@ from scale_deformable_attention_forward_gb300 import inputs as gen  # noqa: E402
 METRIC = "MSDA fwd+bwd Gsamples/s (q·h·l·p) and achieved HBM GB/s vs GB300 peak"
 UNIT = "Gsamples/s"
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_SOURCES = ["msda_kernels.cuh", "msda_launch.cuh", "msda_api.cu", "msda_forward_f32.cu",
-                  "msda_forward_bf16.cu", "msda_backward_f32.cu", "msda_backward_bf16.cu"]
+CSRC = os.path.join(ROOT, "scale_deformable_attention_forward_gb300", "csrc")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")
 
 
@@ -66,9 +65,9 @@ def compulsory_bytes(w: gen.Workload):
 
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, "scale_deformable_attention_forward_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+    for f in sorted(os.listdir(CSRC)):
+        with open(os.path.join(CSRC, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
 
 

@@ -3,6 +3,7 @@
 // (accumulator zero-fill and binary32 -> bfloat16 conversion).
 #include "msda.h"
 #include "msda_kernels.cuh"
+#include "msda_shape.cuh"
 
 #include <limits.h>
 #include <string.h>
@@ -52,53 +53,63 @@ int validate_desc(const msda_desc *d) {
     // 32-bit index limits (stated in msda.h)
     if (d->N_h > 0 && d->C_h > 0 && d->L > kIndexLimit / d->N_h / d->C_h) return MSDA_ERR_TOO_LARGE;
     const int64_t nlp = d->N_l * d->N_p;
-    if (d->N_p >= 16384) return MSDA_ERR_TOO_LARGE;
+    // Corner offsets of cells up to two pixels outside a level are formed in
+    // 32-bit arithmetic: (L + 2*max(W) + 4) * N_h * C_h must stay below 2^31.
+    int64_t wmax = 0;
+    for (int64_t l = 0; l < d->N_l; ++l) wmax = d->spatial_shapes[2 * l + 1] > wmax ? d->spatial_shapes[2 * l + 1] : wmax;
+    if (d->N_h > 0 && d->C_h > 0 && d->L + 2 * wmax + 4 > kIndexLimit / d->N_h / d->C_h) return MSDA_ERR_TOO_LARGE;
     if (d->N_q > 0 && d->N_h > 0 && nlp > 0 && d->N_q > kIndexLimit / 2 / d->N_h / nlp) return MSDA_ERR_TOO_LARGE;
     if (d->B > 0 && d->N_q > 0 && d->N_h > 0 && d->B > kIndexLimit / d->N_q / d->N_h) return MSDA_ERR_TOO_LARGE;
     if (d->loc_dtype != MSDA_DTYPE_F32) return MSDA_ERR_UNSUPPORTED;
     return MSDA_OK;
 }
 
-// Kernel configuration chosen from C_h and pointer alignment.
+// Kernel configuration chosen from C_h, pointer alignment and direction.
 struct Config {
     bool vec;
     int G, NCH;
 };
 
-int next_pow2(int64_t x) {
-    int p = 1;
-    while (p < x) p <<= 1;
-    return p;
-}
-
-int choose_config(const msda_desc *d, bool all_aligned16, Config *cfg) {
-    const int V = d->value_dtype == MSDA_DTYPE_BF16 ? 8 : 4;
-    cfg->vec = all_aligned16 && (d->C_h % V == 0);
+// V: elements per vector access; aligned: every value-typed pointer is
+// aligned to V elements (and the binary32 accumulator to 16 bytes).
+int choose_config(const msda_desc *d, int V, bool aligned_ok, int preferred_lanes, Config *cfg) {
+    cfg->vec = aligned_ok && (d->C_h % V == 0);
     const int64_t chunks = cfg->vec ? d->C_h / V : d->C_h;
-    if (cfg->vec) {
-        cfg->G = next_pow2(chunks < 1 ? 1 : (chunks > 32 ? 32 : chunks));
-    } else {
-        cfg->G = 32;
-    }
-    const int64_t per_lane = (chunks + cfg->G - 1) / cfg->G;
-    cfg->NCH = next_pow2(per_lane < 1 ? 1 : per_lane);
-    if (cfg->NCH > 8) return MSDA_ERR_UNSUPPORTED;
+    if (chunks > 256) return MSDA_ERR_UNSUPPORTED;
+    const msda::Shape s = msda::select_shape((int)chunks, preferred_lanes);
+    cfg->G = s.G;
+    cfg->NCH = s.NCH;
     return MSDA_OK;
 }
 
-Params make_params(const msda_desc *d, const Config &cfg) {
+// n / d in the kernels' FastDiv form (d >= 1).
+msda::FastDiv make_fastdiv(uint32_t d) {
+    msda::FastDiv f;
+    f.d = d < 1 ? 1 : d;
+    uint32_t s = 0;
+    while (((uint64_t)1 << s) < f.d) ++s;
+    f.shift = s;
+    f.mul = (uint32_t)((((uint64_t)1 << 32) * (((uint64_t)1 << s) - f.d)) / f.d + 1);
+    return f;
+}
+
+Params make_params(const msda_desc *d, const Config &cfg, int V_vec) {
     Params p;
     memset(&p, 0, sizeof(p));
     p.rows = (uint32_t)(d->B * d->N_q * d->N_h);
     p.N_q = (int)d->N_q;
     p.N_h = (int)d->N_h;
     p.C_h = (int)d->C_h;
+    p.N_l = (int)d->N_l;
+    p.N_p = (int)d->N_p;
     p.NLP = (int)(d->N_l * d->N_p);
-    p.np_div = d->N_p > 0 ? (((uint64_t)1 << 32) + (uint64_t)d->N_p - 1) / (uint64_t)d->N_p : 0;
-    const int V = cfg.vec ? (d->value_dtype == MSDA_DTYPE_BF16 ? 8 : 4) : 1;
+    const int V = cfg.vec ? V_vec : 1;
     p.chunks = (int)(d->C_h / V);
-    p.row_order_bhq = 1;
+    p.div_q = make_fastdiv((uint32_t)d->N_q);
+    p.div_h = make_fastdiv((uint32_t)d->N_h);
+    p.div_p = make_fastdiv((uint32_t)d->N_p);
     p.padding = d->padding_mode;
+    p.flags = 0;
     if (d->value_layout == MSDA_LAYOUT_BLNC) {
         p.v_sB = d->L * d->N_h * d->C_h;
         p.v_sP = (int)(d->N_h * d->C_h);
@@ -129,6 +140,88 @@ Params make_params(const msda_desc *d, const Config &cfg) {
     }
     p.off = d->align_corners ? 0.0f : -0.5f;
     return p;
+}
+
+// Shared memory a block may give to privatised grad_value levels.
+#ifndef MSDA_PRIV_SMEM_BYTES
+#define MSDA_PRIV_SMEM_BYTES (160 * 1024)
+#endif
+
+int sm_count() {
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 0;
+    if (dev < 64 && cached[dev] > 0) return cached[dev];
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    if (dev < 64) cached[dev] = n;
+    return n;
+}
+
+// Backward work split: queries per block, and which levels each block
+// accumulates in shared memory.  A level is privatised (smallest levels first,
+// within MSDA_PRIV_SMEM_BYTES) only if a block adds, on average, at least two
+// corner contributions per privatised pixel: below that the flush costs more
+// atomics than it saves.  Privatising blocks hold one (b, h) and a long run of
+// queries, sized so the blocks fill whole waves of the GPU.
+void plan_backward(const msda_desc *d, const Config &cfg, bool want_gv, int n_sm, Params *p, bool *priv) {
+    const int groups = msda::kBwdThreads / cfg.G;
+    const int64_t BH = d->B * d->N_h;
+    *priv = false;
+    for (int l = 0; l < msda::kMaxLevels; ++l) p->priv_start[l] = -1;
+    p->priv_pixels = 0;
+    p->swizzle = (d->C_h % 32 == 0) ? 1 : 0;
+    int64_t q_chunk = groups;  // one query row per group
+    if (want_gv && cfg.vec && cfg.G <= 8 && d->C_h % 4 == 0 && d->N_l > 0 && n_sm > 0 && BH > 0) {
+        // smallest levels first
+        int order[msda::kMaxLevels];
+        for (int l = 0; l < d->N_l; ++l) order[l] = l;
+        for (int a = 1; a < d->N_l; ++a)
+            for (int b2 = a; b2 > 0 && p->H[order[b2]] * (int64_t)p->W[order[b2]] <
+                                           p->H[order[b2 - 1]] * (int64_t)p->W[order[b2 - 1]]; --b2) {
+                const int t = order[b2]; order[b2] = order[b2 - 1]; order[b2 - 1] = t;
+            }
+        int64_t pixels = 0;
+        int nlev = 0;
+        int start[msda::kMaxLevels];
+        for (int i = 0; i < d->N_l; ++i) {
+            const int l = order[i];
+            const int64_t hw = (int64_t)p->H[l] * p->W[l];
+            if ((pixels + hw) * d->C_h * 4 > MSDA_PRIV_SMEM_BYTES) break;
+            start[l] = (int)pixels;
+            pixels += hw;
+            ++nlev;
+        }
+        if (nlev > 0) {
+            // blocks: one (b, h) and ceil(N_q / chunks) queries each; pick the
+            // chunk count that fills whole waves best, with at least two waves
+            int64_t best = 1;
+            double best_eff = -1.0;
+            for (int64_t c = 1; c <= 256; ++c) {
+                const int64_t blocks = BH * c;
+                if (blocks < 2 * n_sm && c < 256) continue;
+                const int64_t waves = (blocks + n_sm - 1) / n_sm;
+                const double eff = (double)blocks / (double)(waves * n_sm);
+                if (eff > best_eff + 1e-9) {
+                    best_eff = eff;
+                    best = c;
+                }
+                if (blocks >= 8 * n_sm) break;
+            }
+            const int64_t qc = (d->N_q + best - 1) / best;
+            const int64_t adds = qc * d->N_p * nlev * 4;
+            if (qc >= groups && adds >= 2 * pixels) {
+                *priv = true;
+                q_chunk = qc;
+                p->priv_pixels = (int)pixels;
+                for (int i = 0; i < nlev; ++i) p->priv_start[order[i]] = start[order[i]];
+            }
+        }
+    }
+    // at most 65535 query chunks per (b, h) (the grid's y extent)
+    const int64_t min_chunk = (d->N_q + 65534) / 65535;
+    if (q_chunk < min_chunk) q_chunk = ((min_chunk + groups - 1) / groups) * groups;
+    p->q_chunk = (int)(q_chunk < 1 ? 1 : q_chunk);
 }
 
 }  // namespace
@@ -209,10 +302,13 @@ int msda_forward(const msda_desc *desc, const void *value, const void *sampling_
         !aligned(attention_weights, 4))
         return MSDA_ERR_MISALIGNED;
     Config cfg;
-    rc = choose_config(d, aligned(value, 16) && aligned(out, 16), &cfg);
+    const int V = d->value_dtype == MSDA_DTYPE_BF16 ? msda::VecWidth<__nv_bfloat16>::value
+                                                     : msda::VecWidth<float>::value;
+    rc = choose_config(d, V, aligned(value, V * es) && aligned(out, V * es), MSDA_FWD_LANES, &cfg);
     if (rc) return rc;
     if (out_elems == 0) return MSDA_OK;
-    const Params p = make_params(d, cfg);
+    Params p = make_params(d, cfg, V);
+    p.n_sm = sm_count();
     cudaError_t e;
     if (d->value_dtype == MSDA_DTYPE_F32)
         e = msda::launch_forward<float>(p, cfg.vec, cfg.G, cfg.NCH, (const float *)value,
@@ -268,27 +364,32 @@ int msda_backward(const msda_desc *desc, const void *grad_output, const void *va
     }
     float *acc = fv ? (bf16 ? (float *)workspace : (float *)grad_value) : nullptr;
     Config cfg;
-    rc = choose_config(d,
-                       aligned(grad_output, 16) && aligned(value, 16) && (!fv || aligned(acc, 16)),
-                       &cfg);
+    const int V = d->value_dtype == MSDA_DTYPE_BF16 ? msda::BwdVecWidth<__nv_bfloat16>::value
+                                                     : msda::BwdVecWidth<float>::value;
+    rc = choose_config(d, V,
+                       aligned(grad_output, V * es) && aligned(value, V * es) && (!fv || aligned(acc, 16)),
+                       MSDA_BWD_LANES, &cfg);
     if (rc) return rc;
-    const Params p = make_params(d, cfg);
-    const int flags = (fv ? msda::kGradValue : 0) | (fl ? msda::kGradLoc : 0) | (fa ? msda::kGradAttn : 0);
+    Params p = make_params(d, cfg, V);
+    p.flags = (fv ? msda::kGradValue : 0) | (fl ? msda::kGradLoc : 0) | (fa ? msda::kGradAttn : 0);
+    bool priv = false;
+    p.n_sm = samples > 0 ? sm_count() : 0;
+    plan_backward(d, cfg, fv != 0, p.n_sm, &p, &priv);
 
     cudaError_t e = cudaSuccess;
     if (fv) e = msda::launch_zero_f32(acc, value_elems, stream);
     if (e == cudaSuccess && samples > 0) {
         if (bf16)
             e = msda::launch_backward<__nv_bfloat16>(
-                p, cfg.vec, cfg.G, cfg.NCH, (const __nv_bfloat16 *)grad_output, (const __nv_bfloat16 *)value,
+                p, cfg.vec, cfg.G, cfg.NCH, priv, (const __nv_bfloat16 *)grad_output, (const __nv_bfloat16 *)value,
                 (const float *)sampling_locations, (const float *)attention_weights, acc,
-                (float *)grad_sampling_locations, (float *)grad_attention_weights, flags, stream);
+                (float *)grad_sampling_locations, (float *)grad_attention_weights, stream);
         else
-            e = msda::launch_backward<float>(p, cfg.vec, cfg.G, cfg.NCH, (const float *)grad_output,
+            e = msda::launch_backward<float>(p, cfg.vec, cfg.G, cfg.NCH, priv, (const float *)grad_output,
                                              (const float *)value, (const float *)sampling_locations,
                                              (const float *)attention_weights, acc,
                                              (float *)grad_sampling_locations, (float *)grad_attention_weights,
-                                             flags, stream);
+                                             stream);
     }
     if (e == cudaSuccess && fv && bf16)
         e = msda::launch_f32_to_bf16(acc, (__nv_bfloat16 *)grad_value, value_elems, stream);

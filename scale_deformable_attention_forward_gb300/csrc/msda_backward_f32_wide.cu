@@ -1,0 +1,8 @@
+// Backward kernels: f32 value tensors, vector path, wide rows (padding read at run time).
+#include "msda_launch.cuh"
+
+namespace msda {
+template cudaError_t launch_backward_pad<float, -2>(const Params &, int, int, bool, const float *, const float *,
+                                                  const float *, const float *, float *, float *, float *,
+                                                  cudaStream_t);
+}  // namespace msda

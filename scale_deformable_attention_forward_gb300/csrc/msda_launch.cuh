@@ -1,68 +1,136 @@
 // msda_launch.cuh -- host-side launchers: pick the kernel instantiation for
-// (vector width, lanes per sample G, channel chunks per lane NCH).
+// (vector width, lanes per row G, channel chunks per lane NCH, padding,
+// backward outputs).
 #pragma once
 
 #include "msda_kernels.cuh"
+#include "msda_shape.cuh"
 
 namespace msda {
 
-template <typename T> struct VecWidth;
-template <> struct VecWidth<float> { static constexpr int value = 4; };          // 16-byte loads
-template <> struct VecWidth<__nv_bfloat16> { static constexpr int value = 8; };  // 16-byte loads
+inline unsigned grid_for(uint32_t rows, int G) {
+    const uint64_t threads = (uint64_t)rows * (uint64_t)G;
+    return (unsigned)((threads + kThreads - 1) / kThreads);
+}
 
-inline unsigned grid_for_rows(uint32_t rows) { return (rows + (kThreads / 32) - 1) / (kThreads / 32); }
+#define MSDA_SHAPES(X)                                                                            \
+    X(1, 1) X(2, 1) X(2, 2) X(2, 4) X(2, 8) X(4, 1) X(4, 2) X(4, 4) X(4, 8) X(8, 1) X(8, 2) X(8, 4) \
+    X(8, 8) X(16, 1) X(16, 2) X(16, 4) X(16, 8) X(32, 1) X(32, 2) X(32, 4) X(32, 8)
 
-// Instantiated combinations: vector path G in {1..32} with NCH 1, G = 32 with
-// NCH in {2,4,8}; scalar path G = 32 with NCH in {1,2,4,8}.
-#define MSDA_VECTOR_CASES(X) X(1, 1) X(2, 1) X(4, 1) X(8, 1) X(16, 1) X(32, 1) X(32, 2) X(32, 4) X(32, 8)
-#define MSDA_SCALAR_CASES(X) X(32, 1) X(32, 2) X(32, 4) X(32, 8)
+// Blocks of a kernel that fit on one multiprocessor at once (0 if unknown).
+template <typename K>
+int resident_blocks(K kernel, int threads, size_t smem) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem) != cudaSuccess) return 0;
+    return n;
+}
 
-template <typename T>
-cudaError_t launch_forward(const Params &p, bool vec, int G, int NCH, const T *value, const float *loc,
-                           const float *attn, T *out, cudaStream_t stream) {
-    if (p.rows == 0) return cudaSuccess;
-    const dim3 grid(grid_for_rows(p.rows)), block(kThreads);
-    constexpr int V = VecWidth<T>::value;
-#define MSDA_FWD_V(GG, NN)                                                                        \
-    if (vec && G == GG && NCH == NN) {                                                            \
-        msda_forward_kernel<T, V, GG, NN><<<grid, block, 0, stream>>>(p, value, loc, attn, out);  \
-        return cudaGetLastError();                                                                \
+// The forward's blocks loop over rows: launch no more than fit at once.
+template <typename T, int V, int GG, int NN, int PAD>
+cudaError_t fwd_launch(const Params &p, const T *value, const float *loc, const float *attn, T *out,
+                       cudaStream_t stream) {
+    auto kernel = msda_forward_kernel<T, V, GG, NN, PAD>;
+    unsigned blocks = grid_for(p.rows, GG);
+    const int per_sm = resident_blocks(kernel, kThreads, 0);
+    if (per_sm > 0 && p.n_sm > 0 && (uint64_t)per_sm * p.n_sm < blocks) blocks = (unsigned)(per_sm * p.n_sm);
+    kernel<<<blocks, kThreads, 0, stream>>>(p, value, loc, attn, out);
+    return cudaGetLastError();
+}
+
+template <typename T, int V, int GG, int NN>
+cudaError_t fwd_shape(const Params &p, const T *value, const float *loc, const float *attn, T *out,
+                      cudaStream_t stream) {
+    if constexpr (V > 1 && specialised_shape(GG, NN)) {
+        if (p.padding == 0) return fwd_launch<T, V, GG, NN, 0>(p, value, loc, attn, out, stream);
+        return fwd_launch<T, V, GG, NN, 1>(p, value, loc, attn, out, stream);
+    } else {
+        return fwd_launch<T, V, GG, NN, -1>(p, value, loc, attn, out, stream);
     }
-#define MSDA_FWD_S(GG, NN)                                                                        \
-    if (!vec && G == GG && NCH == NN) {                                                           \
-        msda_forward_kernel<T, 1, GG, NN><<<grid, block, 0, stream>>>(p, value, loc, attn, out);  \
-        return cudaGetLastError();                                                                \
+}
+
+// Forward kernels of the vector (VECTOR = true) or scalar path; each
+// (dtype, path) pair is instantiated in its own translation unit.
+template <typename T, bool VECTOR>
+cudaError_t launch_forward_path(const Params &p, int G, int NCH, const T *value, const float *loc,
+                                const float *attn, T *out, cudaStream_t stream) {
+    constexpr int V = VECTOR ? VecWidth<T>::value : 1;
+#define MSDA_FWD_CASE(GG, NN)                                                                     \
+    if constexpr (reachable(GG, NN, MSDA_FWD_LANES)) {                                            \
+        if (G == GG && NCH == NN) return fwd_shape<T, V, GG, NN>(p, value, loc, attn, out, stream); \
     }
-    MSDA_VECTOR_CASES(MSDA_FWD_V)
-    MSDA_SCALAR_CASES(MSDA_FWD_S)
-#undef MSDA_FWD_V
-#undef MSDA_FWD_S
+    MSDA_SHAPES(MSDA_FWD_CASE)
+#undef MSDA_FWD_CASE
     return cudaErrorInvalidConfiguration;
 }
 
-template <typename T>
-cudaError_t launch_backward(const Params &p, bool vec, int G, int NCH, const T *grad_out, const T *value,
-                            const float *loc, const float *attn, float *gv_acc, float *grad_loc,
-                            float *grad_attn, int flags, cudaStream_t stream) {
-    if (p.rows == 0) return cudaSuccess;
-    const dim3 grid(grid_for_rows(p.rows)), block(kThreads);
-    constexpr int V = VecWidth<T>::value;
-#define MSDA_BWD_V(GG, NN)                                                                        \
-    if (vec && G == GG && NCH == NN) {                                                            \
-        msda_backward_kernel<T, V, GG, NN><<<grid, block, 0, stream>>>(                           \
-            p, grad_out, value, loc, attn, gv_acc, grad_loc, grad_attn, flags);                   \
-        return cudaGetLastError();                                                                \
+template <typename T, int V, int GG, int NN, int PAD, int FL, bool PRIV>
+cudaError_t bwd_launch(const Params &p, const T *grad_out, const T *value, const float *loc, const float *attn,
+                       float *gv_acc, float *grad_loc, float *grad_attn, cudaStream_t stream) {
+    const dim3 grid((unsigned)(p.rows / (uint32_t)p.N_q), (unsigned)((p.N_q + p.q_chunk - 1) / p.q_chunk));
+    const dim3 block(kBwdThreads);
+    size_t smem = 0;
+    auto kernel = msda_backward_kernel<T, V, GG, NN, PAD, FL, PRIV>;
+    if constexpr (PRIV) {
+        smem = (size_t)p.priv_pixels * (size_t)p.C_h * sizeof(float);
+        const cudaError_t e =
+            cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
     }
-#define MSDA_BWD_S(GG, NN)                                                                        \
-    if (!vec && G == GG && NCH == NN) {                                                           \
-        msda_backward_kernel<T, 1, GG, NN><<<grid, block, 0, stream>>>(                           \
-            p, grad_out, value, loc, attn, gv_acc, grad_loc, grad_attn, flags);                   \
-        return cudaGetLastError();                                                                \
+    kernel<<<grid, block, smem, stream>>>(p, grad_out, value, loc, attn, gv_acc, grad_loc, grad_attn);
+    return cudaGetLastError();
+}
+
+template <typename T, int V, int GG, int NN, int PAD>
+cudaError_t bwd_flags(const Params &p, bool priv, const T *grad_out, const T *value, const float *loc,
+                      const float *attn, float *gv_acc, float *grad_loc, float *grad_attn, cudaStream_t stream) {
+    constexpr int ALL = kGradValue | kGradLoc | kGradAttn;
+#define MSDA_BWD(FL, PR) \
+    return bwd_launch<T, V, GG, NN, PAD, FL, PR>(p, grad_out, value, loc, attn, gv_acc, grad_loc, grad_attn, stream)
+    if constexpr (PAD < 0 || !specialised_shape(GG, NN)) {
+        MSDA_BWD(-1, false);
+    } else {
+        if constexpr (GG <= 8) {
+            if (priv) {
+                if (p.flags == ALL) MSDA_BWD(ALL, true);
+                if (p.flags == kGradValue) MSDA_BWD(kGradValue, true);
+                MSDA_BWD(-1, true);
+            }
+        }
+        if (p.flags == ALL) MSDA_BWD(ALL, false);
+        if (p.flags == kGradValue) MSDA_BWD(kGradValue, false);
+        if (!(p.flags & kGradValue)) MSDA_BWD(kGradLoc | kGradAttn, false);
+        MSDA_BWD(-1, false);
     }
-    MSDA_VECTOR_CASES(MSDA_BWD_V)
-    MSDA_SCALAR_CASES(MSDA_BWD_S)
-#undef MSDA_BWD_V
-#undef MSDA_BWD_S
+#undef MSDA_BWD
+}
+
+// Backward kernels for one padding specialisation, each (dtype, PAD) pair
+// instantiated in its own translation unit so the library builds in parallel:
+//   PAD 0 / 1: vector path, zeros / border, specialised shapes (wide shapes are
+//              passed on to PAD -2);
+//   PAD -2   : vector path, wide shapes, padding and outputs read at run time;
+//   PAD -1   : scalar path (unaligned pointers or C_h not a multiple of 4).
+template <typename T, int PAD>
+cudaError_t launch_backward_pad(const Params &p, int G, int NCH, bool priv, const T *grad_out, const T *value,
+                                const float *loc, const float *attn, float *gv_acc, float *grad_loc,
+                                float *grad_attn, cudaStream_t stream) {
+    constexpr int V = PAD == -1 ? 1 : BwdVecWidth<T>::value;
+#define MSDA_BWD_CASE(GG, NN)                                                                     \
+    if constexpr (reachable(GG, NN, MSDA_BWD_LANES)) {                                            \
+        if (G == GG && NCH == NN) {                                                               \
+            if constexpr (PAD == -1 || (PAD == -2) != specialised_shape(GG, NN))                  \
+                return bwd_flags<T, V, GG, NN, PAD>(p, PAD < 0 ? false : priv, grad_out, value,   \
+                                                    loc, attn, gv_acc, grad_loc, grad_attn,       \
+                                                    stream);                                      \
+            else if constexpr (PAD >= 0)                                                          \
+                return launch_backward_pad<T, -2>(p, G, NCH, false, grad_out, value, loc, attn,   \
+                                                  gv_acc, grad_loc, grad_attn, stream);           \
+            else                                                                                  \
+                return cudaErrorInvalidConfiguration;                                             \
+        }                                                                                         \
+    }
+    MSDA_SHAPES(MSDA_BWD_CASE)
+#undef MSDA_BWD_CASE
     return cudaErrorInvalidConfiguration;
 }
 
