@@ -129,9 +129,19 @@ typedef struct msda_desc {
 int msda_forward(const msda_desc *desc, const void *value, const void *sampling_locations,
                  const void *attention_weights, void *out, cudaStream_t stream);
 
-/* Bytes of device workspace msda_backward needs: B*L*N_h*C_h*4 (a binary32
- * accumulator for grad_value) when compute_grad_value is set and value_dtype
- * is BF16, else 0.  Returns 0 for an invalid descriptor. */
+/* Bytes of device workspace msda_backward needs, 0 when compute_grad_value is
+ * 0.  With compute_grad_value set it is the sum of (each part starting at a
+ * 256-byte boundary of the workspace):
+ *   - B*L*N_h*C_h*4, a binary32 grad_value accumulator, when value_dtype is
+ *     BF16;
+ *   - when the problem has at least two samples per bilinear cell on average
+ *     (S = B*N_q*N_h*N_l*N_p >= 2*K with K = B*N_h*sum_l (H_l+1)*(W_l+1) cell
+ *     keys, and S < 2^31): (2K+1)*4 bytes of cell counts and cursors, 4 bytes
+ *     per 4096 keys of scan partials and 16*S bytes of per-cell sample
+ *     lists, used to sum grad_value per cell when grad_value is the only
+ *     requested output.
+ * The size depends on the descriptor and the flag only.  Returns 0 for an
+ * invalid descriptor. */
 size_t msda_backward_workspace_size(const msda_desc *desc, int compute_grad_value);
 
 /* Backward ("MS Deformable Attention Backward Kernel API Reference",
@@ -154,7 +164,8 @@ size_t msda_backward_workspace_size(const msda_desc *desc, int compute_grad_valu
  *                       msda_backward_workspace_size(desc, compute_grad_value)
  *                       bytes (NULL when that is 0), 16-byte aligned; its
  *                       contents on entry do not matter.
- * grad_value is accumulated with binary32 atomics, so its summation order
+ * grad_value is accumulated in binary32 with atomic adds (per corner and
+ * sample, or per cell of samples grouped by cell), so its summation order
  * (and last-bit rounding) varies from run to run.
  * Returns MSDA_OK or a negative msda_status. */
 int msda_backward(const msda_desc *desc, const void *grad_output, const void *value,

@@ -2,6 +2,7 @@
 // kernel parameter set-up and dispatch, plus the two small helper kernels
 // (accumulator zero-fill and binary32 -> bfloat16 conversion).
 #include "msda.h"
+#include "msda_entry.h"
 #include "msda_kernels.cuh"
 #include "msda_shape.cuh"
 
@@ -108,6 +109,7 @@ Params make_params(const msda_desc *d, const Config &cfg, int V_vec) {
     p.div_q = make_fastdiv((uint32_t)d->N_q);
     p.div_h = make_fastdiv((uint32_t)d->N_h);
     p.div_p = make_fastdiv((uint32_t)d->N_p);
+    p.div_nlp = make_fastdiv((uint32_t)(d->N_l * d->N_p));
     p.padding = d->padding_mode;
     p.flags = 0;
     if (d->value_layout == MSDA_LAYOUT_BLNC) {
@@ -139,13 +141,36 @@ Params make_params(const msda_desc *d, const Config &cfg, int V_vec) {
         p.sy[l] = (float)(d->align_corners ? H - 1 : H);
     }
     p.off = d->align_corners ? 0.0f : -0.5f;
+    // cell keys: (H_l + 1) x (W_l + 1) per level and (b, h); the reduction
+    // takes the levels with the fewest pixels (longest lists) first
+    int64_t K = 0;
+    for (int64_t l = 0; l < d->N_l; ++l) {
+        p.kst[l] = (int)K;
+        K += (d->spatial_shapes[2 * l] + 1) * (d->spatial_shapes[2 * l + 1] + 1);
+    }
+    // (used only by the cell-sorted grad_value, which plan_backward allows
+    // only when nkeys fits in 31 bits)
+    p.K_bh = K < INT32_MAX ? (int)K : 0;
+    p.nkeys = d->B * d->N_h * K < INT32_MAX ? (uint32_t)(d->B * d->N_h * K) : 0u;
+    int order[msda::kMaxLevels];
+    for (int l = 0; l < (int)d->N_l; ++l) order[l] = l;
+    for (int a = 1; a < (int)d->N_l; ++a)
+        for (int b = a; b > 0 && (int64_t)p.H[order[b]] * p.W[order[b]] < (int64_t)p.H[order[b - 1]] * p.W[order[b - 1]];
+             --b) {
+            const int t = order[b];
+            order[b] = order[b - 1];
+            order[b - 1] = t;
+        }
+    uint32_t end = 0;
+    for (int i = 0; i < (int)d->N_l; ++i) {
+        const int l = order[i];
+        p.ilev[i] = l;
+        end += (uint32_t)(d->B * d->N_h * (int64_t)(p.H[l] + 1) * (p.W[l] + 1));
+        p.iend[i] = end;
+    }
+    p.capacity = (uint32_t)(d->B * d->N_q * d->N_h * d->N_l * d->N_p);
     return p;
 }
-
-// Shared memory a block may give to privatised grad_value levels.
-#ifndef MSDA_PRIV_SMEM_BYTES
-#define MSDA_PRIV_SMEM_BYTES (160 * 1024)
-#endif
 
 int sm_count() {
     static int cached[64] = {0};
@@ -158,70 +183,55 @@ int sm_count() {
     return n;
 }
 
-// Backward work split: queries per block, and which levels each block
-// accumulates in shared memory.  A level is privatised (smallest levels first,
-// within MSDA_PRIV_SMEM_BYTES) only if a block adds, on average, at least two
-// corner contributions per privatised pixel: below that the flush costs more
-// atomics than it saves.  Privatising blocks hold one (b, h) and a long run of
-// queries, sized so the blocks fill whole waves of the GPU.
-void plan_backward(const msda_desc *d, const Config &cfg, bool want_gv, int n_sm, Params *p, bool *priv) {
-    const int groups = msda::kBwdThreads / cfg.G;
-    const int64_t BH = d->B * d->N_h;
-    *priv = false;
-    for (int l = 0; l < msda::kMaxLevels; ++l) p->priv_start[l] = -1;
-    p->priv_pixels = 0;
-    p->swizzle = (d->C_h % 32 == 0) ? 1 : 0;
-    int64_t q_chunk = groups;  // one query row per group
-    if (want_gv && cfg.vec && cfg.G <= 8 && d->C_h % 4 == 0 && d->N_l > 0 && n_sm > 0 && BH > 0) {
-        // smallest levels first
-        int order[msda::kMaxLevels];
-        for (int l = 0; l < d->N_l; ++l) order[l] = l;
-        for (int a = 1; a < d->N_l; ++a)
-            for (int b2 = a; b2 > 0 && p->H[order[b2]] * (int64_t)p->W[order[b2]] <
-                                           p->H[order[b2 - 1]] * (int64_t)p->W[order[b2 - 1]]; --b2) {
-                const int t = order[b2]; order[b2] = order[b2 - 1]; order[b2 - 1] = t;
-            }
-        int64_t pixels = 0;
-        int nlev = 0;
-        int start[msda::kMaxLevels];
-        for (int i = 0; i < d->N_l; ++i) {
-            const int l = order[i];
-            const int64_t hw = (int64_t)p->H[l] * p->W[l];
-            if ((pixels + hw) * d->C_h * 4 > MSDA_PRIV_SMEM_BYTES) break;
-            start[l] = (int)pixels;
-            pixels += hw;
-            ++nlev;
-        }
-        if (nlev > 0) {
-            // blocks: one (b, h) and ceil(N_q / chunks) queries each; pick the
-            // chunk count that fills whole waves best, with at least two waves
-            int64_t best = 1;
-            double best_eff = -1.0;
-            for (int64_t c = 1; c <= 256; ++c) {
-                const int64_t blocks = BH * c;
-                if (blocks < 2 * n_sm && c < 256) continue;
-                const int64_t waves = (blocks + n_sm - 1) / n_sm;
-                const double eff = (double)blocks / (double)(waves * n_sm);
-                if (eff > best_eff + 1e-9) {
-                    best_eff = eff;
-                    best = c;
-                }
-                if (blocks >= 8 * n_sm) break;
-            }
-            const int64_t qc = (d->N_q + best - 1) / best;
-            const int64_t adds = qc * d->N_p * nlev * 4;
-            if (qc >= groups && adds >= 2 * pixels) {
-                *priv = true;
-                q_chunk = qc;
-                p->priv_pixels = (int)pixels;
-                for (int i = 0; i < nlev; ++i) p->priv_start[order[i]] = start[order[i]];
-            }
-        }
+// Workspace of the backward, in 256-byte aligned regions:
+//   acc      binary32 grad_value accumulator (bfloat16 value with grad_value)
+//   offsets  cell-key counts, then offsets (nkeys + 1 int32)   \
+//   cursor   append positions (nkeys int32)                     |  cell-sorted
+//   tiles    tile sums of the scan                              |  grad_value
+//   entries  the samples grouped by cell (samples x 16 bytes)  /
+// The cell-sorted regions are planned when there are at least
+// MSDA_SORT_MIN_DENSITY samples per cell key on average (below that the
+// count, scan and per-key pass cost more than the atomics they save) and the
+// 32-bit entry indices cover the samples.  They are used when grad_value is
+// the only output: next to the value gather of the other two gradients, the
+// sort's own scattered atomics (one count and one append per sample) cost
+// more than the direct per-corner atomics they replace.
+#ifndef MSDA_SORT_MIN_DENSITY
+#define MSDA_SORT_MIN_DENSITY 2
+#endif
+struct BwdPlan {
+    bool sort;
+    size_t acc_off, offsets_off, cursor_off, tiles_off, entries_off, total;
+};
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+BwdPlan plan_backward(const msda_desc *d, int compute_grad_value, bool allow_sort) {
+    BwdPlan w;
+    memset(&w, 0, sizeof(w));
+    if (!compute_grad_value) return w;
+    const int64_t samples = d->B * d->N_q * d->N_h * d->N_l * d->N_p;
+    int64_t K = 0;
+    for (int64_t l = 0; l < d->N_l; ++l) K += (d->spatial_shapes[2 * l] + 1) * (d->spatial_shapes[2 * l + 1] + 1);
+    const int64_t nkeys = d->B * d->N_h * K;
+    w.sort = allow_sort && samples > 0 && samples >= (int64_t)MSDA_SORT_MIN_DENSITY * nkeys &&
+             samples < (int64_t)INT32_MAX &&
+             nkeys + 1 < (int64_t)INT32_MAX;
+    size_t end = 0;  // end of the regions so far (each region starts 256-byte aligned)
+    if (d->value_dtype == MSDA_DTYPE_BF16) {
+        w.acc_off = 0;
+        end = (size_t)(d->B * d->L * d->N_h * d->C_h) * sizeof(float);
     }
-    // at most 65535 query chunks per (b, h) (the grid's y extent)
-    const int64_t min_chunk = (d->N_q + 65534) / 65535;
-    if (q_chunk < min_chunk) q_chunk = ((min_chunk + groups - 1) / groups) * groups;
-    p->q_chunk = (int)(q_chunk < 1 ? 1 : q_chunk);
+    if (w.sort) {
+        const int64_t tiles = (nkeys + msda::kScanTile - 1) / msda::kScanTile;
+        w.offsets_off = align256(end);
+        w.cursor_off = align256(w.offsets_off + (size_t)(nkeys + 1) * sizeof(int));
+        w.tiles_off = align256(w.cursor_off + (size_t)nkeys * sizeof(int));
+        w.entries_off = align256(w.tiles_off + (size_t)(tiles > 0 ? tiles : 1) * sizeof(int));
+        end = w.entries_off + (size_t)samples * 16;
+    }
+    w.total = end;
+    return w;
 }
 
 }  // namespace
@@ -261,6 +271,95 @@ __global__ void msda_f32_to_bf16_kernel(const float *__restrict__ acc, __nv_bflo
     }
 }
 
+__device__ __forceinline__ int block_exclusive_scan(int x, int *warp_sums, int *total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int incl = x;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) warp_sums[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        int w = lane < (int)(blockDim.x >> 5) ? warp_sums[lane] : 0;
+        int wi = w;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, wi, o);
+            if (lane >= o) wi += y;
+        }
+        warp_sums[lane] = wi - w;  // exclusive
+        if (lane == 31) *total = wi;
+    }
+    __syncthreads();
+    return warp_sums[warp] + incl - x;
+}
+
+__global__ void __launch_bounds__(kScanThreads)
+msda_scan_tiles_kernel(const int *__restrict__ counts, uint32_t n, int *__restrict__ tile_sums) {
+    __shared__ int red[kScanThreads / 32];
+    const uint64_t base = (uint64_t)blockIdx.x * kScanTile + (uint64_t)threadIdx.x * kScanPer;
+    int s = 0;
+#pragma unroll
+    for (int i = 0; i < kScanPer; ++i)
+        if (base + i < n) s += counts[base + i];
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = s;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        int t = red[threadIdx.x];
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+        if (threadIdx.x == 0) tile_sums[blockIdx.x] = t;
+    }
+}
+
+__global__ void __launch_bounds__(kScanThreads)
+msda_scan_apply_kernel(int *__restrict__ offsets, uint32_t n, const int *__restrict__ tile_sums,
+                       int *__restrict__ cursor) {
+    __shared__ int warp_sums[32];
+    __shared__ int total;
+    __shared__ int prefix;
+    // sum of the tiles before this one
+    int pre = 0;
+    for (uint32_t t = threadIdx.x; t < blockIdx.x; t += kScanThreads) pre += tile_sums[t];
+    {
+        const int lane = threadIdx.x & 31;
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) pre += __shfl_xor_sync(0xffffffffu, pre, o);
+        if (lane == 0) warp_sums[threadIdx.x >> 5] = pre;
+        __syncthreads();
+        if (threadIdx.x < 32) {
+            int t = warp_sums[threadIdx.x];
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+            if (threadIdx.x == 0) prefix = t;
+        }
+        __syncthreads();
+    }
+    const uint64_t base = (uint64_t)blockIdx.x * kScanTile + (uint64_t)threadIdx.x * kScanPer;
+    int v[kScanPer];
+    int s = 0;
+#pragma unroll
+    for (int i = 0; i < kScanPer; ++i) {
+        v[i] = base + i < n ? offsets[base + i] : 0;
+        s += v[i];
+    }
+    const int ex = block_exclusive_scan(s, warp_sums, &total) + prefix;
+    int run = ex;
+#pragma unroll
+    for (int i = 0; i < kScanPer; ++i) {
+        if (base + i < n) {
+            offsets[base + i] = run;
+            cursor[base + i] = run;
+        }
+        run += v[i];
+    }
+    if (blockIdx.x == gridDim.x - 1 && threadIdx.x == 0) offsets[n] = prefix + total;
+}
+
 static unsigned helper_grid(int64_t n, int per_thread) {
     const int64_t threads = (n + per_thread - 1) / per_thread;
     int64_t blocks = (threads + 255) / 256;
@@ -279,6 +378,122 @@ cudaError_t launch_f32_to_bf16(const float *acc, __nv_bfloat16 *out, int64_t n, 
     if (n <= 0) return cudaSuccess;
     msda_f32_to_bf16_kernel<<<helper_grid(n, 8), 256, 0, stream>>>(acc, out, n);
     return cudaGetLastError();
+}
+
+cudaError_t launch_sort_keys(const Params &p, const float *loc, const BwdBuffers &bb, cudaStream_t stream) {
+    if (p.nkeys == 0) return cudaSuccess;
+    cudaError_t e = launch_zero_f32(reinterpret_cast<float *>(bb.offsets), (int64_t)p.nkeys + 1, stream);
+    if (e != cudaSuccess) return e;
+    const uint64_t samples = (uint64_t)p.rows * (uint64_t)p.NLP;
+    if (samples > 0) {
+        uint64_t blocks = (samples + 1023) / 1024;  // 4 samples a thread
+        const uint64_t cap = (uint64_t)(p.n_sm > 0 ? p.n_sm : 152) * 8;  // grid-stride beyond a few waves
+        if (blocks > cap) blocks = cap;
+        if (p.padding == 0)
+            msda_count_kernel<0><<<(unsigned)blocks, 256, 0, stream>>>(p, loc, bb.offsets);
+        else
+            msda_count_kernel<1><<<(unsigned)blocks, 256, 0, stream>>>(p, loc, bb.offsets);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    const unsigned tiles = (unsigned)(((uint64_t)p.nkeys + kScanTile - 1) / kScanTile);
+    msda_scan_tiles_kernel<<<tiles, kScanThreads, 0, stream>>>(bb.offsets, p.nkeys, bb.tile_sums);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    msda_scan_apply_kernel<<<tiles, kScanThreads, 0, stream>>>(bb.offsets, p.nkeys, bb.tile_sums, bb.cursor);
+    return cudaGetLastError();
+}
+
+
+size_t backward_workspace_bytes(const msda_desc *desc, int compute_grad_value, bool allow_sort) {
+    if (validate_desc(desc) != MSDA_OK) return 0;
+    return plan_backward(desc, compute_grad_value, allow_sort).total;
+}
+
+int backward_entry(const msda_desc *desc, const void *grad_output, const void *value,
+                   const void *sampling_locations, const void *attention_weights, int compute_grad_value,
+                   int compute_grad_sampling_locations, int compute_grad_attention_weights, void *grad_value,
+                   void *grad_sampling_locations, void *grad_attention_weights, void *workspace,
+                   size_t workspace_bytes, bool allow_sort, cudaStream_t stream) {
+    int rc = validate_desc(desc);
+    if (rc) return rc;
+    const msda_desc *d = desc;
+    const int fv = compute_grad_value, fl = compute_grad_sampling_locations, fa = compute_grad_attention_weights;
+    if ((fv != 0 && fv != 1) || (fl != 0 && fl != 1) || (fa != 0 && fa != 1)) return MSDA_ERR_BAD_ENUM;
+    if (!fv && !fl && !fa) return MSDA_ERR_NO_OUTPUT;  // backward page: at least one flag must be True
+    const int64_t samples = d->B * d->N_q * d->N_h * d->N_l * d->N_p;
+    const int64_t value_elems = d->B * d->L * d->N_h * d->C_h;
+    const int64_t go_elems = d->B * d->N_q * d->N_h * d->C_h;
+    const bool need_v = (fl || fa) && samples > 0 && d->C_h > 0;
+    const bool need_a = (fv || fl) && samples > 0;
+    if (samples > 0 && !sampling_locations) return MSDA_ERR_NULL_POINTER;
+    if (samples > 0 && go_elems > 0 && !grad_output) return MSDA_ERR_NULL_POINTER;
+    if (need_v && !value) return MSDA_ERR_NULL_POINTER;
+    if (need_a && !attention_weights) return MSDA_ERR_NULL_POINTER;
+    if (fv && value_elems > 0 && !grad_value) return MSDA_ERR_NULL_POINTER;
+    if (fl && samples > 0 && !grad_sampling_locations) return MSDA_ERR_NULL_POINTER;
+    if (fa && samples > 0 && !grad_attention_weights) return MSDA_ERR_NULL_POINTER;
+    const size_t es = value_elem_size(d);
+    if (!aligned(grad_output, es) || !aligned(value, es) || !aligned(grad_value, es) ||
+        !aligned(sampling_locations, 4) || !aligned(attention_weights, 4) ||
+        !aligned(grad_sampling_locations, 4) || !aligned(grad_attention_weights, 4))
+        return MSDA_ERR_MISALIGNED;
+    const bool bf16 = d->value_dtype == MSDA_DTYPE_BF16;
+    const BwdPlan plan = plan_backward(d, fv, allow_sort);
+    if (plan.total > 0) {
+        if (workspace_bytes < plan.total) return MSDA_ERR_WORKSPACE;
+        if (!workspace) return MSDA_ERR_NULL_POINTER;
+        if (!aligned(workspace, 16)) return MSDA_ERR_MISALIGNED;
+    }
+    unsigned char *ws = (unsigned char *)workspace;
+    BwdBuffers bb;
+    memset(&bb, 0, sizeof(bb));
+    bb.gv_acc = fv ? (bf16 ? (float *)(ws + plan.acc_off) : (float *)grad_value) : nullptr;
+    bb.grad_loc = (float *)grad_sampling_locations;
+    bb.grad_attn = (float *)grad_attention_weights;
+    if (plan.sort) {
+        bb.offsets = (int *)(ws + plan.offsets_off);
+        bb.cursor = (int *)(ws + plan.cursor_off);
+        bb.tile_sums = (int *)(ws + plan.tiles_off);
+        bb.entries = (uint4 *)(ws + plan.entries_off);
+    }
+    Config cfg;
+    const int V = BwdVecWidth<float>::value;
+    rc = choose_config(d, V,
+                       aligned(grad_output, V * es) && aligned(value, V * es) && (!fv || aligned(bb.gv_acc, 16)),
+                       MSDA_BWD_LANES, &cfg);
+    if (rc) return rc;
+    Params p = make_params(d, cfg, V);
+    p.flags = (fv ? kGradValue : 0) | (fl ? kGradLoc : 0) | (fa ? kGradAttn : 0);
+    p.n_sm = samples > 0 ? sm_count() : 0;
+
+    cudaError_t e = cudaSuccess;
+    if (fv) e = launch_zero_f32(bb.gv_acc, value_elems, stream);
+    const bool sort = plan.sort && !fl && !fa;
+    if (e == cudaSuccess && samples > 0 && sort) e = launch_sort_keys(p, (const float *)sampling_locations, bb, stream);
+    if (e == cudaSuccess && samples > 0) {
+        if (bf16)
+            e = launch_backward<__nv_bfloat16>(p, cfg.vec, cfg.G, cfg.NCH, sort,
+                                               (const __nv_bfloat16 *)grad_output, (const __nv_bfloat16 *)value,
+                                               (const float *)sampling_locations, (const float *)attention_weights,
+                                               bb, stream);
+        else
+            e = launch_backward<float>(p, cfg.vec, cfg.G, cfg.NCH, sort, (const float *)grad_output,
+                                       (const float *)value, (const float *)sampling_locations,
+                                       (const float *)attention_weights, bb, stream);
+    }
+    if (e == cudaSuccess && samples > 0 && sort) {
+        if (bf16)
+            e = cfg.vec ? launch_gv_reduce<__nv_bfloat16, true>(p, cfg.G, cfg.NCH,
+                                                                (const __nv_bfloat16 *)grad_output, bb, stream)
+                        : launch_gv_reduce<__nv_bfloat16, false>(p, cfg.G, cfg.NCH,
+                                                                 (const __nv_bfloat16 *)grad_output, bb, stream);
+        else
+            e = cfg.vec ? launch_gv_reduce<float, true>(p, cfg.G, cfg.NCH, (const float *)grad_output, bb, stream)
+                        : launch_gv_reduce<float, false>(p, cfg.G, cfg.NCH, (const float *)grad_output, bb, stream);
+    }
+    if (e == cudaSuccess && fv && bf16) e = launch_f32_to_bf16(bb.gv_acc, (__nv_bfloat16 *)grad_value, value_elems, stream);
+    return record_cuda(e);
 }
 
 }  // namespace msda
@@ -322,9 +537,7 @@ int msda_forward(const msda_desc *desc, const void *value, const void *sampling_
 }
 
 size_t msda_backward_workspace_size(const msda_desc *desc, int compute_grad_value) {
-    if (validate_desc(desc) != MSDA_OK) return 0;
-    if (!compute_grad_value || desc->value_dtype != MSDA_DTYPE_BF16) return 0;
-    return (size_t)(desc->B * desc->L * desc->N_h * desc->C_h) * sizeof(float);
+    return msda::backward_workspace_bytes(desc, compute_grad_value, true);
 }
 
 int msda_backward(const msda_desc *desc, const void *grad_output, const void *value,
@@ -332,68 +545,10 @@ int msda_backward(const msda_desc *desc, const void *grad_output, const void *va
                   int compute_grad_sampling_locations, int compute_grad_attention_weights, void *grad_value,
                   void *grad_sampling_locations, void *grad_attention_weights, void *workspace,
                   size_t workspace_bytes, cudaStream_t stream) {
-    int rc = validate_desc(desc);
-    if (rc) return rc;
-    const msda_desc *d = desc;
-    const int fv = compute_grad_value, fl = compute_grad_sampling_locations, fa = compute_grad_attention_weights;
-    if ((fv != 0 && fv != 1) || (fl != 0 && fl != 1) || (fa != 0 && fa != 1)) return MSDA_ERR_BAD_ENUM;
-    if (!fv && !fl && !fa) return MSDA_ERR_NO_OUTPUT;  // backward page: at least one flag must be True
-    const int64_t samples = d->B * d->N_q * d->N_h * d->N_l * d->N_p;
-    const int64_t value_elems = d->B * d->L * d->N_h * d->C_h;
-    const int64_t go_elems = d->B * d->N_q * d->N_h * d->C_h;
-    const bool need_v = (fl || fa) && samples > 0 && d->C_h > 0;
-    const bool need_a = (fv || fl) && samples > 0;
-    if (samples > 0 && !sampling_locations) return MSDA_ERR_NULL_POINTER;
-    if (samples > 0 && go_elems > 0 && !grad_output) return MSDA_ERR_NULL_POINTER;
-    if (need_v && !value) return MSDA_ERR_NULL_POINTER;
-    if (need_a && !attention_weights) return MSDA_ERR_NULL_POINTER;
-    if (fv && value_elems > 0 && !grad_value) return MSDA_ERR_NULL_POINTER;
-    if (fl && samples > 0 && !grad_sampling_locations) return MSDA_ERR_NULL_POINTER;
-    if (fa && samples > 0 && !grad_attention_weights) return MSDA_ERR_NULL_POINTER;
-    const size_t es = value_elem_size(d);
-    if (!aligned(grad_output, es) || !aligned(value, es) || !aligned(grad_value, es) ||
-        !aligned(sampling_locations, 4) || !aligned(attention_weights, 4) ||
-        !aligned(grad_sampling_locations, 4) || !aligned(grad_attention_weights, 4))
-        return MSDA_ERR_MISALIGNED;
-    const bool bf16 = d->value_dtype == MSDA_DTYPE_BF16;
-    const size_t ws_need = msda_backward_workspace_size(d, fv);
-    if (ws_need > 0) {
-        if (workspace_bytes < ws_need) return MSDA_ERR_WORKSPACE;
-        if (!workspace) return MSDA_ERR_NULL_POINTER;
-        if (!aligned(workspace, 16)) return MSDA_ERR_MISALIGNED;
-    }
-    float *acc = fv ? (bf16 ? (float *)workspace : (float *)grad_value) : nullptr;
-    Config cfg;
-    const int V = d->value_dtype == MSDA_DTYPE_BF16 ? msda::BwdVecWidth<__nv_bfloat16>::value
-                                                     : msda::BwdVecWidth<float>::value;
-    rc = choose_config(d, V,
-                       aligned(grad_output, V * es) && aligned(value, V * es) && (!fv || aligned(acc, 16)),
-                       MSDA_BWD_LANES, &cfg);
-    if (rc) return rc;
-    Params p = make_params(d, cfg, V);
-    p.flags = (fv ? msda::kGradValue : 0) | (fl ? msda::kGradLoc : 0) | (fa ? msda::kGradAttn : 0);
-    bool priv = false;
-    p.n_sm = samples > 0 ? sm_count() : 0;
-    plan_backward(d, cfg, fv != 0, p.n_sm, &p, &priv);
-
-    cudaError_t e = cudaSuccess;
-    if (fv) e = msda::launch_zero_f32(acc, value_elems, stream);
-    if (e == cudaSuccess && samples > 0) {
-        if (bf16)
-            e = msda::launch_backward<__nv_bfloat16>(
-                p, cfg.vec, cfg.G, cfg.NCH, priv, (const __nv_bfloat16 *)grad_output, (const __nv_bfloat16 *)value,
-                (const float *)sampling_locations, (const float *)attention_weights, acc,
-                (float *)grad_sampling_locations, (float *)grad_attention_weights, stream);
-        else
-            e = msda::launch_backward<float>(p, cfg.vec, cfg.G, cfg.NCH, priv, (const float *)grad_output,
-                                             (const float *)value, (const float *)sampling_locations,
-                                             (const float *)attention_weights, acc,
-                                             (float *)grad_sampling_locations, (float *)grad_attention_weights,
-                                             stream);
-    }
-    if (e == cudaSuccess && fv && bf16)
-        e = msda::launch_f32_to_bf16(acc, (__nv_bfloat16 *)grad_value, value_elems, stream);
-    return record_cuda(e);
+    return msda::backward_entry(desc, grad_output, value, sampling_locations, attention_weights, compute_grad_value,
+                                compute_grad_sampling_locations, compute_grad_attention_weights, grad_value,
+                                grad_sampling_locations, grad_attention_weights, workspace, workspace_bytes, true,
+                                stream);
 }
 
 const char *msda_status_string(int status) {

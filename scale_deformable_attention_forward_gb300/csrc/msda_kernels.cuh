@@ -44,12 +44,14 @@ struct FastDiv {
     }
 };
 
-// Everything a kernel needs, passed by value (kernel parameter space).
+// Everything a kernel needs, passed by value (kernel parameter space; the
+// kernels take it as __grid_constant__, so per-level entries indexed by a
+// warp-uniform level are read from the constant bank without a local copy).
 struct Params {
     uint32_t rows;  // B * N_h * N_q, ordered (b, h, q)
     int N_q, N_h, C_h, N_l, N_p, NLP;
     int chunks;     // C_h / VEC: channel chunks per row
-    FastDiv div_q, div_h, div_p;  // by N_q, N_h, N_p
+    FastDiv div_q, div_h, div_p, div_nlp;  // by N_q, N_h, N_p, N_l * N_p
     int padding;    // 0 zeros, 1 border (used when the kernel is not specialised)
     int flags;      // kGradValue | kGradLoc | kGradAttn (backward)
     // value (and grad_value / accumulator) element strides
@@ -62,12 +64,14 @@ struct Params {
     int H[kMaxLevels], W[kMaxLevels], start[kMaxLevels];
     float sx[kMaxLevels], sy[kMaxLevels];  // pixels per unit of normalised coordinate
     float off;                             // -0.5 (align_corners = 0) or 0 (align_corners = 1)
-    // backward: queries per block, and the levels accumulated in shared memory
-    int q_chunk;
-    int priv_start[kMaxLevels];  // first shared-memory pixel of a privatised level, -1 if not
-    int priv_pixels;             // privatised pixels in total (C_h floats each)
-    int swizzle;                 // rotate channels by pixel within 32-float runs (C_h % 32 == 0)
-    int n_sm;                    // multiprocessors of the device (grid sizing)
+    int n_sm;                              // multiprocessors of the device (grid sizing)
+    // cell-sorted grad_value (see the sorting kernels below)
+    int K_bh;                   // cell keys of one (b, h): sum over levels of (H_l + 1) * (W_l + 1)
+    int kst[kMaxLevels];        // first key of level l inside a (b, h)
+    uint32_t nkeys;             // B * N_h * K_bh
+    uint32_t capacity;          // entries the workspace holds (= samples)
+    int ilev[kMaxLevels];       // reduction order of the levels (fewest pixels first)
+    uint32_t iend[kMaxLevels];  // running end of the reduction's keys, per position in that order
 };
 
 enum : int { kGradValue = 1, kGradLoc = 2, kGradAttn = 4 };
@@ -234,115 +238,154 @@ __device__ __forceinline__ Cell make_cell(float u, float v, float sx, float sy, 
     return c;
 }
 
-// ---------------------------------------------------------------- forward
-// Level tables copied to shared memory once per block: lanes of a warp look
-// up different levels at the same time, which shared memory serves in one
-// pass (the kernel parameter space would serialise distinct addresses).
+// ---------------------------------------------------------------- shared by the row kernels
+// Level tables copied to shared memory once per block: the lanes of a warp
+// look up different levels at once, which shared memory serves in one pass.
 struct LevelTables {
-    int W[kMaxLevels], H[kMaxLevels], start[kMaxLevels], priv[kMaxLevels];
+    int W[kMaxLevels], H[kMaxLevels], start[kMaxLevels], kst[kMaxLevels];
     float sx[kMaxLevels], sy[kMaxLevels];
 };
-
 __device__ __forceinline__ void load_level_tables(const Params &p, LevelTables &t) {
     if (threadIdx.x < (unsigned)p.N_l) {
         const int l = threadIdx.x;
         t.W[l] = p.W[l];
         t.H[l] = p.H[l];
         t.start[l] = p.start[l];
-        t.priv[l] = p.priv_start[l];
+        t.kst[l] = p.kst[l];
         t.sx[l] = p.sx[l];
         t.sy[l] = p.sy[l];
     }
     __syncthreads();
 }
 
-// Corner offsets and weights of one sample, as the consumers of a group read
-// them: corner i reads value at element offset off[i] (relative to the
-// (b, h) slice) with weight w[i].  A corner that reads nothing ("zeros"
-// padding outside the map) gets weight 0 and an offset clamped onto the map,
-// so every corner can be loaded without a branch.  Non-finite numbers stored
-// at such a clamped pixel would reach the sum as 0 * inf; the pages leave
-// non-finite inputs unspecified.
-struct alignas(16) CornerRec {
-    int off[4];
+// Corner reads and weights of one sample.  o[i] is the element offset
+// (relative to the (b, h) slice of value) of corner i = (0,0), (0,1), (1,0),
+// (1,1) (row, column) of the cell, clamped onto the map, so that every corner
+// can be loaded without a branch; w[i] is the bilinear weight times A, 0 for
+// a corner outside the map ("zeros").  (Non-finite numbers stored at such a
+// clamped pixel would reach the sum as 0 * inf; the pages leave non-finite
+// inputs unspecified.)  The weights are formed as ay_i * ax_k with
+// ax0 = A(1-fx), ax1 = A fx, ay0 = 1-fy, ay1 = fy.
+struct Corners {
+    int o[4];
     float w[4];
 };
 
-__device__ __forceinline__ void corner_offsets(const Cell &c, int W, int H, int start, int sP, int (&off)[4]) {
+__device__ __forceinline__ Corners corners_of(const Cell &c, float A, int W, int H, int start, int sP) {
     const int xa = min(max(c.x0, 0), W - 1), xb = min(max(c.x0 + 1, 0), W - 1);
     const int ya = min(max(c.y0, 0), H - 1), yb = min(max(c.y0 + 1, 0), H - 1);
+    Corners k;
     const int ra = start + ya * W, rb = start + yb * W;
-    off[0] = (ra + xa) * sP;
-    off[1] = (ra + xb) * sP;
-    off[2] = (rb + xa) * sP;
-    off[3] = (rb + xb) * sP;
+    k.o[0] = (ra + xa) * sP;
+    k.o[1] = (ra + xb) * sP;
+    k.o[2] = (rb + xa) * sP;
+    k.o[3] = (rb + xb) * sP;
+    const float A1 = A * c.fx;
+    const float ax0 = A - A1, ax1 = A1, ay0 = 1.0f - c.fy, ay1 = c.fy;
+    k.w[0] = (c.valid & 1u) ? ay0 * ax0 : 0.0f;
+    k.w[1] = (c.valid & 2u) ? ay0 * ax1 : 0.0f;
+    k.w[2] = (c.valid & 4u) ? ay1 * ax0 : 0.0f;
+    k.w[3] = (c.valid & 8u) ? ay1 * ax1 : 0.0f;
+    return k;
 }
 
-// A group of G lanes owns one row at a time.  Its samples are taken G at a
-// time: lane r computes the bilinear cell of sample j0 + r (the cell
-// arithmetic is done once per sample) and writes the sample's CornerRec to
-// shared memory; then the group walks the G samples together, reads each
-// record with two 16-byte shared loads and loads every corner's channel row
-// with one instruction, two samples' corners before their multiply-adds.
-// Blocks stay resident and loop over rows; while a group works on a row the
-// locations and weights of its next row are already being fetched.
+// Per-warp exchange of sample records through shared memory.  A group of G
+// lanes owns one row; lane r computes the record of the row's sample j0 + r
+// and the group then reads the G records back one sample at a time.  Records
+// are two 16-byte halves kept in two arrays; record (group g, sample s) sits
+// at position g*G + (s ^ f(g)) of the warp's 32, with f chosen so that the
+// groups of a warp reading sample s at the same time hit distinct 16-byte
+// bank slots (one wavefront per read), while each group's stores fill its own
+// G positions (contiguous, one wavefront per 128 bytes).
+template <int G> __device__ __forceinline__ int rec_pos(int g, int s) {
+    if constexpr (G >= 8) return g * G + (s ^ g);
+    else if constexpr (G == 4) return g * G + (s ^ ((g >> 1) & 3));
+    else return g * G + s;
+}
+
+// Rows of a block: the blocks (as many as fit on the GPU at once) sweep the
+// rows together, GPB consecutive rows per block and step, so at any time the
+// whole GPU works on one window of neighbouring queries: value lines are
+// shared in L2 by the multiprocessors and in L1 by a block's groups.  (Giving
+// each block its own contiguous run of rows measured slower.)
+struct RowRange {
+    uint32_t beg, end, step;
+};
+template <int GPB>
+__device__ __forceinline__ RowRange block_rows(const Params &p) {
+    RowRange rr;
+    rr.beg = blockIdx.x * GPB;
+    rr.end = p.rows;
+    rr.step = gridDim.x * GPB;
+    return rr;
+}
+
+// ---------------------------------------------------------------- forward
+#ifndef MSDA_FWD_MIN_BLOCKS
+#define MSDA_FWD_MIN_BLOCKS 3
+#endif
+// Blocks per SM the row kernels are compiled for (registers a thread: 85 for
+// rows of up to 8 elements a lane, 128 for the wide-row kernels).
+__host__ __device__ constexpr int row_min_blocks(int elems) { return elems <= 8 ? MSDA_FWD_MIN_BLOCKS : 2; }
+
+// One sample's cell in the form the lanes of a group exchange (six 32-bit
+// shuffles): o0 is the element offset (relative to the (b, h) slice of value)
+// of the top-left corner read, with bit 31 set when the right-hand corners
+// read the next pixel to the right (clear when both columns clamp onto the
+// same pixel; offsets are below 2^31), o1 the offset of the bottom-left
+// corner read, and ax0 = A(1-fx), ax1 = A fx, ay0 = 1-fy, ay1 = fy the
+// separable weight factors, each 0 when its column or row lies outside the
+// map ("zeros"): corner (i, k) gets ay_i * ax_k.
+struct FwdCell {
+    int o0, o1;
+    float ax0, ax1, ay0, ay1;
+};
+
+__device__ __forceinline__ FwdCell fwd_cell(const Cell &c, float A, int W, int H, int start, int sP) {
+    const int xa = min(max(c.x0, 0), W - 1), xb = min(max(c.x0 + 1, 0), W - 1);
+    const int ya = min(max(c.y0, 0), H - 1), yb = min(max(c.y0 + 1, 0), H - 1);
+    FwdCell f;
+    f.o0 = (int)((unsigned)((start + ya * W + xa) * sP) | ((unsigned)(xb - xa) << 31));
+    f.o1 = (start + yb * W + xa) * sP;
+    const float A1 = A * c.fx;
+    f.ax0 = (c.valid & 5u) ? A - A1 : 0.0f;  // column x0 lies in the map
+    f.ax1 = (c.valid & 10u) ? A1 : 0.0f;     // column x0 + 1
+    f.ay0 = (c.valid & 3u) ? 1.0f - c.fy : 0.0f;
+    f.ay1 = (c.valid & 12u) ? c.fy : 0.0f;
+    return f;
+}
+
+// A group of G lanes owns one row (b, q, h) at a time; a block's groups take
+// consecutive rows of its run, so the rows in flight on a multiprocessor are
+// neighbouring queries of one head and reuse value lines in L1.  The row's
+// samples are taken G at a time: lane r loads sample j0 + r's location and
+// weight (coalesced) and computes its bilinear cell once; the group then
+// walks the G samples, receiving each cell from its owner by shuffles, and
+// loads every corner's channel row with one instruction per channel chunk
+// (lane r owns chunks r, r+G, ...), two samples' corners in flight.
 // PAD: 0 zeros, 1 border, -1 read p.padding at run time.
 template <typename T, int VEC, int G, int NCH, int PAD>
-__global__ void __launch_bounds__(kThreads, 3)
-msda_forward_kernel(const Params p, const T *__restrict__ value, const float *__restrict__ loc,
+__global__ void __launch_bounds__(kThreads, row_min_blocks(NCH *VEC))
+msda_forward_kernel(const __grid_constant__ Params p, const T *__restrict__ value, const float *__restrict__ loc,
                     const float *__restrict__ attn, T *__restrict__ out) {
     __shared__ LevelTables lt;
-    __shared__ CornerRec recs[kThreads];  // one record per lane: [warp][s][group]
     load_level_tables(p, lt);
-    constexpr int GPB = kThreads / G;  // groups (rows in flight) per block
+    constexpr int GPB = kThreads / G;  // rows in flight per block
     const int lane = threadIdx.x & 31;
     const int r = lane & (G - 1);
-    const int grp = lane / G;
-    const unsigned gmask = G == 32 ? 0xffffffffu : (((1u << G) - 1u) << (lane & ~(G - 1)));
-    CornerRec *wrec = recs + (threadIdx.x & ~31);  // sample s of group g at s * (32 / G) + g
-    CornerRec &mine = wrec[r * (32 / G) + grp];
-    const int sP = p.v_sP, sJ = p.l_sJ, sXY = p.l_sXY;
+    const int base = lane & ~(G - 1);
+    const unsigned gmask = G == 32 ? 0xffffffffu : (((1u << G) - 1u) << base);
+    const int sP = p.v_sP, sJ = p.l_sJ, sXY = p.l_sXY, NLP = p.NLP;
     int nk = 0;  // chunks this lane owns: k*G + r < chunks
 #pragma unroll
     for (int k = 0; k < NCH; ++k) nk += (k * G + r < p.chunks);
-    constexpr int PF = 2;  // samples of a row whose inputs are prefetched per lane (batches 0 and 1)
-    static_assert(PF == 2, "the owner phase below selects between two prefetched samples");
-    const uint64_t stride = (uint64_t)gridDim.x * GPB;
+    const RowRange rr = block_rows<GPB>(p);
 
-    // inputs of this lane's first PF samples of a row
-    auto fetch = [&](uint64_t row64, float (&u)[PF], float (&v)[PF], float (&A)[PF]) {
-        if (row64 < p.rows) {
-            const Row rw = decode_row(p, (uint32_t)row64);
-            const float *lp = loc + rw.b * p.l_sB +
-                              (int64_t)((rw.q * (uint32_t)p.N_h + rw.h) * (uint32_t)p.NLP) * sJ;
-            const float *ap = attn + (int64_t)rw.bqh * p.NLP;
-#pragma unroll
-            for (int t = 0; t < PF; ++t) {
-                const int j = r + t * G;
-                if (j < p.NLP) {
-                    u[t] = __ldg(lp + j * sJ);
-                    v[t] = __ldg(lp + j * sJ + sXY);
-                    A[t] = __ldg(ap + j);
-                }
-            }
-        }
-    };
-    float nu[PF], nv[PF], nA[PF];
-    uint64_t row64 = (uint64_t)blockIdx.x * GPB + threadIdx.x / G;
-    fetch(row64, nu, nv, nA);
-    for (; row64 < p.rows; row64 += stride) {
-        float cu[PF], cv[PF], cA[PF];
-#pragma unroll
-        for (int t = 0; t < PF; ++t) {
-            cu[t] = nu[t];
-            cv[t] = nv[t];
-            cA[t] = nA[t];
-        }
-        fetch(row64 + stride, nu, nv, nA);
-        const Row rw = decode_row(p, (uint32_t)row64);
+    for (uint32_t row = rr.beg + threadIdx.x / G; row < rr.end; row += rr.step) {
+        const Row rw = decode_row(p, row);
         const T *vbh = value + rw.b * p.v_sB + (int64_t)rw.h * p.v_sH + r * VEC;
-        const float *lp = loc + rw.b * p.l_sB + (int64_t)((rw.q * (uint32_t)p.N_h + rw.h) * (uint32_t)p.NLP) * sJ;
-        const float *ap = attn + (int64_t)rw.bqh * p.NLP;
+        const float *lp = loc + rw.b * p.l_sB + (int64_t)((rw.q * (uint32_t)p.N_h + rw.h) * (uint32_t)NLP) * sJ;
+        const float *ap = attn + (int64_t)rw.bqh * NLP;
 
         float acc[NCH][VEC];
 #pragma unroll
@@ -350,73 +393,62 @@ msda_forward_kernel(const Params p, const T *__restrict__ value, const float *__
 #pragma unroll
             for (int e = 0; e < VEC; ++e) acc[k][e] = 0.0f;
 
-        for (int j0 = 0, t = 0; j0 < p.NLP; j0 += G, ++t) {
-            // owner phase: this lane's sample
-            {
-                CornerRec rec;
-                const int j = j0 + r;
-                if (j < p.NLP) {
-                    const int l = (int)p.div_p.div((uint32_t)j);
-                    const int W = lt.W[l], H = lt.H[l];
-                    float u, v, A;
-                    if (t < PF) {  // prefetched
-                        u = t == 0 ? cu[0] : cu[PF - 1];
-                        v = t == 0 ? cv[0] : cv[PF - 1];
-                        A = t == 0 ? cA[0] : cA[PF - 1];
-                    } else {
-                        u = __ldg(lp + j * sJ);
-                        v = __ldg(lp + j * sJ + sXY);
-                        A = __ldg(ap + j);
-                    }
-                    const Cell c = make_cell<PAD>(u, v, lt.sx[l], lt.sy[l], p.off, W, H, p.padding);
-                    const float ax = A - A * c.fx, bx = A * c.fx;  // A(1-fx), A fx
-                    const float gy = 1.0f - c.fy;
-                    rec.w[0] = (c.valid & 1u) ? ax * gy : 0.0f;
-                    rec.w[1] = (c.valid & 2u) ? bx * gy : 0.0f;
-                    rec.w[2] = (c.valid & 4u) ? ax * c.fy : 0.0f;
-                    rec.w[3] = (c.valid & 8u) ? bx * c.fy : 0.0f;
-                    corner_offsets(c, W, H, lt.start[l], sP, rec.off);
-                } else {  // past the last sample: four zero-weight reads of pixel 0
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        rec.off[i] = 0;
-                        rec.w[i] = 0.0f;
-                    }
-                }
-                mine = rec;
+        for (int j0 = 0; j0 < NLP; j0 += G) {
+            // owner phase: this lane's sample (past the last sample: weight 0 at offset 0)
+            FwdCell mine = {0, 0, 0.0f, 0.0f, 0.0f, 0.0f};
+            const int j = j0 + r;
+            if (j < NLP) {
+                const float u = __ldg(lp + j * sJ), v = __ldg(lp + j * sJ + sXY), A = __ldg(ap + j);
+                const int l = (int)p.div_p.div((uint32_t)j);
+                const int W = lt.W[l], H = lt.H[l];
+                const Cell c = make_cell<PAD>(u, v, lt.sx[l], lt.sy[l], p.off, W, H, p.padding);
+                mine = fwd_cell(c, A, W, H, lt.start[l], sP);
             }
-            __syncwarp(gmask);
-            // consume phase: the group's G samples, two at a time
-            // two samples' corners in flight when a lane's share of a corner is
-            // at most 4 floats, else one (register budget)
-            constexpr int S2 = (G >= 2 && NCH * VEC <= 4) ? 2 : 1;
+            // consume phase: the group's samples in order, corners of two in flight
+            const int ns = min(G, NLP - j0);
+            constexpr int S2 = (G >= 2 && NCH * VEC <= 8) ? 2 : 1;
 #pragma unroll
             for (int s = 0; s < G; s += S2) {
-                CornerRec rec[S2];
-                float x[S2][4][NCH][VEC];
+                if (s < ns) {
+                    int o[S2][4];
+                    float w[S2][4];
+                    float x[S2][4][NCH][VEC];
 #pragma unroll
-                for (int h2 = 0; h2 < S2; ++h2) {
-                    rec[h2] = wrec[(s + h2) * (32 / G) + grp];
+                    for (int h2 = 0; h2 < S2; ++h2) {
+                        const int src = base + s + h2;
+                        const int o0 = __shfl_sync(gmask, mine.o0, src);
+                        const int o1 = __shfl_sync(gmask, mine.o1, src);
+                        const float ax0 = __shfl_sync(gmask, mine.ax0, src);
+                        const float ax1 = __shfl_sync(gmask, mine.ax1, src);
+                        const float ay0 = __shfl_sync(gmask, mine.ay0, src);
+                        const float ay1 = __shfl_sync(gmask, mine.ay1, src);
+                        const int dx = (int)((unsigned)o0 >> 31) * sP;
+                        o[h2][0] = o0 & 0x7fffffff;
+                        o[h2][1] = (o0 & 0x7fffffff) + dx;
+                        o[h2][2] = o1;
+                        o[h2][3] = o1 + dx;
+                        w[h2][0] = ay0 * ax0;
+                        w[h2][1] = ay0 * ax1;
+                        w[h2][2] = ay1 * ax0;
+                        w[h2][3] = ay1 * ax1;
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const T *src = vbh + rec[h2].off[i];
+                        for (int i = 0; i < 4; ++i)
 #pragma unroll
-                        for (int k = 0; k < NCH; ++k)
-                            if (k < nk) VecIO<T, VEC>::load(src + k * G * VEC, x[h2][i][k]);
+                            for (int k = 0; k < NCH; ++k)
+                                if (k < nk) VecIO<T, VEC>::load(vbh + o[h2][i] + k * G * VEC, x[h2][i][k]);
                     }
+#pragma unroll
+                    for (int h2 = 0; h2 < S2; ++h2)
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+#pragma unroll
+                            for (int k = 0; k < NCH; ++k)
+                                if (k < nk)
+#pragma unroll
+                                    for (int e = 0; e < VEC; ++e)
+                                        acc[k][e] = fmaf(w[h2][i], x[h2][i][k][e], acc[k][e]);
                 }
-#pragma unroll
-                for (int h2 = 0; h2 < S2; ++h2)
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-#pragma unroll
-                        for (int k = 0; k < NCH; ++k)
-                            if (k < nk)
-#pragma unroll
-                                for (int e = 0; e < VEC; ++e)
-                                    acc[k][e] = fmaf(rec[h2].w[i], x[h2][i][k][e], acc[k][e]);
             }
-            __syncwarp(gmask);  // records are rewritten by the next batch
         }
         T *dst = out + (int64_t)rw.bqh * p.C_h + r * VEC;
 #pragma unroll
@@ -426,8 +458,6 @@ msda_forward_kernel(const Params p, const T *__restrict__ value, const float *__
 }
 
 // ---------------------------------------------------------------- backward
-constexpr int kBwdThreads = 512;
-
 // Sum each of a lane's G per-sample partials over the G lanes of its group so
 // that lane r ends with the total of sample r (a transposed butterfly: at
 // each step a lane keeps half of its entries and sends the other half to its
@@ -447,91 +477,77 @@ __device__ __forceinline__ float reduce_scatter(float (&v)[G], int r, unsigned g
     return v[0];
 }
 
-// Shared-memory index of channel c of privatised pixel px.  With C_h a
-// multiple of 32 the channels of a pixel are rotated by the pixel index
-// inside each run of 32 floats, so the groups of a warp that add to
-// different pixels at once spread over the banks.
-__device__ __forceinline__ int priv_index(int px, int c, int C_h, int swz) {
-    return px * C_h + (swz ? ((c & ~31) | ((c + px) & 31)) : c);
+// A sample's cell key for the cell-sorted grad_value: the cell's top-left
+// corner (y0, x0), y0 in [-1, H-1], x0 in [-1, W-1], numbered row-major on a
+// (H+1) x (W+1) grid after the keys of the levels before it; -1 when none of
+// the cell's corners lies in the map ("zeros" beyond the edge), such a sample
+// adds nothing to grad_value.
+__device__ __forceinline__ int cell_key(const Cell &c, int W, int kst) {
+    return c.valid ? kst + (c.y0 + 1) * (W + 1) + (c.x0 + 1) : -1;
 }
 
-// What the consumers of a group need of one sample in the backward: the
-// pixels of its four corners (clamped onto the map when a corner reads
-// nothing), the bilinear weights w (0 for such corners) and their derivatives
-// with respect to the pixel coordinates (dwx, dwy; also 0 for such corners),
-// the attention weight, and pdelta = (shared-memory pixel - pixel) when the
-// sample's level is accumulated in shared memory (kNoPriv otherwise).
-constexpr int kNoPriv = -2147483647 - 1;
-struct alignas(16) BwdRec {
-    int pix[4];
-    float w[4], dwx[4], dwy[4];
-    float A;
-    int pdelta;
-    int pad_[2];
-};
-
-// A block owns one (b, h) and the queries [q0, q0 + q_chunk); a group of G
-// lanes owns one query row at a time and walks its samples G at a time, as in
-// the forward: lane r computes sample j0 + r's cell and writes its BwdRec to
-// shared memory, and the group reads each record back and loads each
-// corner's channel row with one instruction.  Per sample and lane it forms
-// the partial dot products d_i of g with the four corners, then
-// <g, S> = sum w_i d_i (grad_attention) and <g, dS/dx> = sum dwx_i d_i,
-// <g, dS/dy> = sum dwy_i d_i (grad_location); a transposed butterfly leaves
-// lane r with sample r's totals, which it stores.  grad_value receives
-// A*w_i*g per corner: into a block-private binary32 copy in shared memory for
-// the privatised (small) levels when PRIV, flushed with vector atomics at the
-// end, else straight into the accumulator with red.global.add.v4.f32.
+// The backward reuses the forward's work split: a group of G lanes per row,
+// samples taken G at a time, lane r computing sample j0 + r's cell once and
+// publishing its record (corner offsets, weights A w_i).  With grad_output's
+// row g in registers (lane r holds its channel chunks), each lane forms, for
+// every sample of the batch, its part of d_i = <g, V_i> at the four corners;
+// a transposed butterfly leaves lane r with sample r's totals, from which it
+// computes, with its own cell's fractions,
+//   <g, S>     = sum_i w_i d_i        -> grad_attention_weights
+//   <g, dS/dx> = sum_i dw_i/dx d_i     -> grad_sampling_locations.x = A sx <g, dS/dx>
+//   <g, dS/dy> = sum_i dw_i/dy d_i     -> grad_sampling_locations.y = A sy <g, dS/dy>
+// (corners outside the map read 0: their d_i count as 0).  grad_value
+// receives A w_i g at corner i:
+//   SORT = false: straight into the binary32 accumulator, one
+//                 red.global.add.v4.f32 per lane and corner;
+//   SORT = true : not here.  The owner lane appends its sample to its cell's
+//                 list (entry = row, A, fx, fy, at a slot taken from the
+//                 cell's cursor); msda_gv_reduce_kernel adds the lists up.
 // FL: kGradValue|kGradLoc|kGradAttn or kGradValue (exactly these outputs),
 // kGradLoc|kGradAttn (no grad_value; the two others as p.flags says), or -1
 // (everything from p.flags at run time).  PAD as in the forward.
-template <typename T, int VEC, int G, int NCH, int PAD, int FL, bool PRIV>
-__global__ void __launch_bounds__(kBwdThreads)
-msda_backward_kernel(const Params p, const T *__restrict__ grad_out, const T *__restrict__ value,
-                     const float *__restrict__ loc, const float *__restrict__ attn,
-                     float *__restrict__ gv_acc, float *__restrict__ grad_loc,
-                     float *__restrict__ grad_attn) {
-    extern __shared__ float s_acc[];
+template <typename T, int VEC, int G, int NCH, int PAD, int FL, bool SORT>
+__global__ void __launch_bounds__(kThreads, row_min_blocks(NCH *VEC))
+msda_backward_kernel(const __grid_constant__ Params p, const T *__restrict__ grad_out, const T *__restrict__ value,
+                     const float *__restrict__ loc, const float *__restrict__ attn, float *__restrict__ gv_acc,
+                     float *__restrict__ grad_loc, float *__restrict__ grad_attn, int *__restrict__ cursor,
+                     uint4 *__restrict__ entries) {
     __shared__ LevelTables lt;
-    __shared__ BwdRec recs[kBwdThreads];  // one record per lane: [warp][s][group]
+    __shared__ int4 rec_o[kThreads];
+    __shared__ float4 rec_w[kThreads];
     load_level_tables(p, lt);
+    constexpr int GPB = kThreads / G;
     const int flags = FL < 0 ? p.flags : (FL == (kGradLoc | kGradAttn) ? (p.flags & FL) : FL);
     const bool want_gv = flags & kGradValue, want_gl = flags & kGradLoc, want_ga = flags & kGradAttn;
     const bool need_v = want_gl || want_ga;  // value is read only for these two
     const bool need_a = want_gv || want_gl;  // attention is read only for these two
-    if constexpr (PRIV) {
-        for (int i = threadIdx.x; i < p.priv_pixels * p.C_h; i += kBwdThreads) s_acc[i] = 0.0f;
-        __syncthreads();
-    }
-
+    const bool scatter = want_gv && !SORT;   // consumers add into grad_value
     const int lane = threadIdx.x & 31;
     const int r = lane & (G - 1);
     const int grp = lane / G;
     const unsigned gmask = G == 32 ? 0xffffffffu : (((1u << G) - 1u) << (lane & ~(G - 1)));
-    BwdRec *wrec = recs + (threadIdx.x & ~31);
-    BwdRec &mine = wrec[r * (32 / G) + grp];
-    const uint32_t bhi = blockIdx.x;  // b * N_h + h
-    const uint32_t b = p.div_h.div(bhi), h = bhi - b * (uint32_t)p.N_h;
-    const uint32_t q0 = blockIdx.y * (uint32_t)p.q_chunk;
-    const uint32_t q1 = min((uint32_t)p.N_q, q0 + (uint32_t)p.q_chunk);
-    const int64_t bhoff = b * p.v_sB + (int64_t)h * p.v_sH;
-    const T *vbh = value + bhoff + r * VEC;
-    float *gbh = gv_acc + bhoff + r * VEC;
-    const int sP = p.v_sP, sJ = p.l_sJ, sXY = p.l_sXY;
+    int4 *wo = rec_o + (threadIdx.x & ~31);
+    float4 *ww = rec_w + (threadIdx.x & ~31);
+    const int mypos = rec_pos<G>(grp, r);
+    const int sP = p.v_sP, sJ = p.l_sJ, sXY = p.l_sXY, NLP = p.NLP;
     int nk = 0;  // chunks this lane owns: k*G + r < chunks
 #pragma unroll
     for (int k = 0; k < NCH; ++k) nk += (k * G + r < p.chunks);
+    const RowRange rr = block_rows<GPB>(p);
 
-    for (uint32_t q = q0 + threadIdx.x / G; q < q1; q += kBwdThreads / G) {
-        const uint32_t bqh = (b * (uint32_t)p.N_q + q) * (uint32_t)p.N_h + h;
-        const int64_t lrow = b * p.l_sB + (int64_t)((q * (uint32_t)p.N_h + h) * (uint32_t)p.NLP) * sJ;
+    for (uint32_t row = rr.beg + threadIdx.x / G; row < rr.end; row += rr.step) {
+        const Row rw = decode_row(p, row);
+        const int64_t bhoff = rw.b * p.v_sB + (int64_t)rw.h * p.v_sH;
+        const T *vbh = value + bhoff + r * VEC;
+        float *gbh = gv_acc + bhoff + r * VEC;
+        const int64_t lrow = rw.b * p.l_sB + (int64_t)((rw.q * (uint32_t)p.N_h + rw.h) * (uint32_t)NLP) * sJ;
         const float *lp = loc + lrow;
         float *glp = grad_loc + lrow;
-        const float *ap = attn + (int64_t)bqh * p.NLP;
-        float *gap = grad_attn + (int64_t)bqh * p.NLP;
+        const float *ap = attn + (int64_t)rw.bqh * NLP;
+        float *gap = grad_attn + (int64_t)rw.bqh * NLP;
         float g[NCH][VEC];
         {
-            const T *src = grad_out + (int64_t)bqh * p.C_h + r * VEC;
+            const T *src = grad_out + (int64_t)rw.bqh * p.C_h + r * VEC;
 #pragma unroll
             for (int k = 0; k < NCH; ++k) {
                 if (k < nk) {
@@ -543,162 +559,279 @@ msda_backward_kernel(const Params p, const T *__restrict__ grad_out, const T *__
             }
         }
 
-        for (int j0 = 0; j0 < p.NLP; j0 += G) {
+        for (int j0 = 0; j0 < NLP; j0 += G) {
             // owner phase: this lane's sample
             const int j = j0 + r;
-            float A = 0.0f, sxk = 0.0f, syk = 0.0f;
+            const bool live = j < NLP;
+            int l = 0;
+            float A = 0.0f;
+            Cell c;
             {
-                BwdRec rec;
-                rec.pdelta = kNoPriv;
-                if (j < p.NLP) {
-                    const int l = (int)p.div_p.div((uint32_t)j);
-                    const int W = lt.W[l], H = lt.H[l];
-                    const float u = __ldg(lp + j * sJ), v = __ldg(lp + j * sJ + sXY);
+                Corners cr = {{0, 0, 0, 0}, {0.0f, 0.0f, 0.0f, 0.0f}};
+                float u = 0.0f, v = 0.0f;
+                if (live) {
+                    l = (int)p.div_p.div((uint32_t)j);
+                    u = __ldg(lp + j * sJ);
+                    v = __ldg(lp + j * sJ + sXY);
                     if (need_a) A = __ldg(ap + j);
-                    const Cell c = make_cell<PAD>(u, v, lt.sx[l], lt.sy[l], p.off, W, H, p.padding);
-                    const int xa = min(max(c.x0, 0), W - 1), xb = min(max(c.x0 + 1, 0), W - 1);
-                    const int ya = min(max(c.y0, 0), H - 1), yb = min(max(c.y0 + 1, 0), H - 1);
-                    const int ra = lt.start[l] + ya * W, rb = lt.start[l] + yb * W;
-                    rec.pix[0] = ra + xa;
-                    rec.pix[1] = ra + xb;
-                    rec.pix[2] = rb + xa;
-                    rec.pix[3] = rb + xb;
-                    const float gx = 1.0f - c.fx, gy = 1.0f - c.fy;
-                    const float w[4] = {gx * gy, c.fx * gy, gx * c.fy, c.fx * c.fy};
-                    const float dwx[4] = {-gy, gy, -c.fy, c.fy};
-                    const float dwy[4] = {-gx, -c.fx, gx, c.fx};
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const bool ok = c.valid & (1u << i);
-                        rec.w[i] = ok ? w[i] : 0.0f;
-                        rec.dwx[i] = ok ? dwx[i] : 0.0f;
-                        rec.dwy[i] = ok ? dwy[i] : 0.0f;
-                    }
-                    rec.A = A;
-                    if constexpr (PRIV) rec.pdelta = lt.priv[l] >= 0 ? lt.priv[l] - lt.start[l] : kNoPriv;
-                    sxk = lt.sx[l] * c.kx;
-                    syk = lt.sy[l] * c.ky;
-                } else {  // past the last sample: zero-weight reads of pixel 0
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        rec.pix[i] = 0;
-                        rec.w[i] = rec.dwx[i] = rec.dwy[i] = 0.0f;
-                    }
-                    rec.A = 0.0f;
                 }
-                mine = rec;
+                const int W = lt.W[l], H = lt.H[l];
+                c = make_cell<PAD>(u, v, lt.sx[l], lt.sy[l], p.off, W, H, p.padding);
+                if (live) cr = corners_of(c, A, W, H, lt.start[l], sP);
+                wo[mypos] = make_int4(cr.o[0], cr.o[1], cr.o[2], cr.o[3]);
+                ww[mypos] = make_float4(cr.w[0], cr.w[1], cr.w[2], cr.w[3]);
+                if constexpr (SORT) {
+                    if (want_gv && live) {
+                        const int key = cell_key(c, W, lt.kst[l]);
+                        if (key >= 0) {
+                            const uint32_t gkey =
+                                (rw.b * (uint32_t)p.N_h + rw.h) * (uint32_t)p.K_bh + (uint32_t)key;
+                            const uint32_t slot = (uint32_t)atomicAdd(cursor + gkey, 1);
+                            if (slot < p.capacity)
+                                entries[slot] = make_uint4(rw.bqh, __float_as_uint(A), __float_as_uint(c.fx),
+                                                           __float_as_uint(c.fy));
+                        }
+                    }
+                }
             }
             __syncwarp(gmask);
-            float pa[G], px[G], py[G];
-            // consume phase: the group's G samples, in order
+            // consume phase: the group's samples in order
+            const int ns = min(G, NLP - j0);
+            float pd[4][G <= 8 ? G : 1];  // this lane's part of d_i, per sample of the batch
+            float dt[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // (G > 8) totals of this lane's own sample
 #pragma unroll
             for (int s = 0; s < G; ++s) {
-                const BwdRec &rec = wrec[s * (32 / G) + grp];
-                int pix[4];
+                float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                if (s < ns) {
+                    const int q = rec_pos<G>(grp, s);
+                    const int4 o4 = wo[q];
+                    const int oo[4] = {o4.x, o4.y, o4.z, o4.w};
+                    if (need_v) {
+                        float x[4][NCH][VEC];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) pix[i] = rec.pix[i];
-                pa[s] = px[s] = py[s] = 0.0f;
-                if (need_v) {
-                    float d[4];  // this lane's part of <g, corner i>
+                        for (int i = 0; i < 4; ++i)
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        d[i] = 0.0f;
-                        const T *src = vbh + pix[i] * sP;
+                            for (int k = 0; k < NCH; ++k)
+                                if (k < nk) VecIO<T, VEC>::load(vbh + oo[i] + k * G * VEC, x[i][k]);
 #pragma unroll
-                        for (int k = 0; k < NCH; ++k) {
-                            if (k < nk) {
-                                float x[VEC];
-                                VecIO<T, VEC>::load(src + k * G * VEC, x);
+                        for (int i = 0; i < 4; ++i)
 #pragma unroll
-                                for (int e = 0; e < VEC; ++e) d[i] = fmaf(g[k][e], x[e], d[i]);
-                            }
-                        }
+                            for (int k = 0; k < NCH; ++k)
+                                if (k < nk)
+#pragma unroll
+                                    for (int e = 0; e < VEC; ++e) d[i] = fmaf(g[k][e], x[i][k][e], d[i]);
                     }
+                    if (scatter) {
+                        const float4 w4 = ww[q];
+                        const float wv[4] = {w4.x, w4.y, w4.z, w4.w};
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        pa[s] = fmaf(rec.w[i], d[i], pa[s]);
-                        px[s] = fmaf(rec.dwx[i], d[i], px[s]);
-                        py[s] = fmaf(rec.dwy[i], d[i], py[s]);
-                    }
-                    if constexpr (G > 8) {  // wide groups: reduce per sample, the owner stores
-                        float ta = pa[s], tx = px[s], ty = py[s];
+                        for (int i = 0; i < 4; ++i)
+                            if (wv[i] != 0.0f)
 #pragma unroll
-                        for (int o = 1; o < G; o <<= 1) {
-                            ta += __shfl_xor_sync(gmask, ta, o);
-                            tx += __shfl_xor_sync(gmask, tx, o);
-                            ty += __shfl_xor_sync(gmask, ty, o);
-                        }
-                        if (r == s && j < p.NLP) {
-                            if (want_ga) gap[j] = ta;
-                            if (want_gl) {
-                                glp[j * sJ] = A * tx * sxk;
-                                glp[j * sJ + sXY] = A * ty * syk;
-                            }
-                        }
+                                for (int k = 0; k < NCH; ++k)
+                                    if (k < nk) RedIO<VEC>::add(gbh + oo[i] + k * G * VEC, g[k], wv[i]);
                     }
                 }
-                if (want_gv) {
-                    const float As = rec.A;
-                    const int pdelta = PRIV ? rec.pdelta : kNoPriv;
+                if constexpr (G <= 8) {
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const float aw = As * rec.w[i];
-                        if (aw != 0.0f) {
-                            if (PRIV && pdelta != kNoPriv) {
-                                const int pxi = pix[i] + pdelta;
+                    for (int i = 0; i < 4; ++i) pd[i][s] = d[i];
+                } else if (need_v) {  // wide groups: sum per sample, the owner keeps it
 #pragma unroll
-                                for (int k = 0; k < NCH; ++k)
-                                    if (k < nk)
+                    for (int o = 1; o < G; o <<= 1)
 #pragma unroll
-                                        for (int e = 0; e < VEC; ++e)
-                                            atomicAdd(&s_acc[priv_index(pxi, (k * G + r) * VEC + e, p.C_h, p.swizzle)],
-                                                      aw * g[k][e]);
-                            } else {
-                                float *dst = gbh + pix[i] * sP;
+                        for (int i = 0; i < 4; ++i) d[i] += __shfl_xor_sync(gmask, d[i], o);
+                    if (r == s) {
 #pragma unroll
-                                for (int k = 0; k < NCH; ++k)
-                                    if (k < nk) RedIO<VEC>::add(dst + k * G * VEC, g[k], aw);
-                            }
-                        }
+                        for (int i = 0; i < 4; ++i) dt[i] = d[i];
                     }
                 }
             }
             __syncwarp(gmask);  // records are rewritten by the next batch
-            if constexpr (G <= 8) {
-                if (need_v) {
-                    const float ta = reduce_scatter<G>(pa, r, gmask);
-                    const float tx = reduce_scatter<G>(px, r, gmask);
-                    const float ty = reduce_scatter<G>(py, r, gmask);
-                    if (j < p.NLP) {
-                        if (want_ga) gap[j] = ta;
-                        if (want_gl) {
-                            glp[j * sJ] = A * tx * sxk;
-                            glp[j * sJ + sXY] = A * ty * syk;
-                        }
+            if (need_v) {
+                if constexpr (G <= 8) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) dt[i] = reduce_scatter<G>(pd[i], r, gmask);
+                }
+                if (live) {
+                    // weights without A and their derivatives; corners outside the map read 0
+                    const float gx = 1.0f - c.fx, gy = 1.0f - c.fy;
+                    const float w[4] = {gx * gy, c.fx * gy, gx * c.fy, c.fx * c.fy};
+                    const float dwx[4] = {-gy, gy, -c.fy, c.fy};
+                    const float dwy[4] = {-gx, -c.fx, gx, c.fx};
+                    float ga = 0.0f, tx = 0.0f, ty = 0.0f;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float di = (c.valid & (1u << i)) ? dt[i] : 0.0f;
+                        ga = fmaf(w[i], di, ga);
+                        tx = fmaf(dwx[i], di, tx);
+                        ty = fmaf(dwy[i], di, ty);
+                    }
+                    if (want_ga) gap[j] = ga;
+                    if (want_gl) {
+                        glp[j * sJ] = A * tx * (lt.sx[l] * c.kx);
+                        glp[j * sJ + sXY] = A * ty * (lt.sy[l] * c.ky);
                     }
                 }
             }
         }
     }
+}
 
-    if constexpr (PRIV) {
-        // Add the block's private levels into the accumulator: one 16-byte
-        // atomic per 4 channels of a pixel, skipping pixels this block never
-        // touched.
-        __syncthreads();
-        const int c4n = p.C_h / 4;
-        float *gb = gv_acc + bhoff;
-        for (int idx = threadIdx.x; idx < p.priv_pixels * c4n; idx += kBwdThreads) {
-            const int pxi = idx / c4n, c = (idx - pxi * c4n) * 4;
-            float v[4];
+// ---------------------------------------------------------------- cell-sorted grad_value
+// grad_value[pixel] = sum over samples s and corners i of s's cell at that
+// pixel of A_s w_i(s) g_{row(s)}.  Scattered one corner at a time this is four
+// C_h-wide atomic adds per sample, and L2's reduction throughput bounds the
+// backward.  Instead the samples are grouped by cell (counting sort on the
+// cell key), and one group of lanes per cell sums its samples' rows of
+// grad_output, weighted for each of the cell's four corners, in registers:
+// one row load per sample, and four atomic adds per cell instead of per
+// sample.
+//   1. msda_count_kernel     counts[key] = samples whose cell is key
+//   2. msda_scan_*_kernel    offsets = exclusive prefix sum of counts;
+//                            cursor = offsets
+//   3. msda_backward_kernel<SORT = true> appends each sample at
+//                            entries[atomicAdd(cursor[key], 1)]
+//   4. msda_gv_reduce_kernel adds the lists into the accumulator
+// Key order within a list is the order of the atomics, so grad_value's
+// summation order (not its value) varies from call to call, as with direct
+// atomics.
+
+// Four consecutive samples per thread, in memory order (b, q, h, l, p): the
+// loads of all four are issued before any key is formed, so each thread has
+// several loads in flight.
+template <int PAD>
+__global__ void __launch_bounds__(256)
+msda_count_kernel(const __grid_constant__ Params p, const float *__restrict__ loc, int *__restrict__ counts) {
+    __shared__ LevelTables lt;
+    load_level_tables(p, lt);
+    constexpr int U = 4;
+    const uint32_t total = p.rows * (uint32_t)p.NLP;
+    const uint32_t per_batch = (uint32_t)p.N_q * (uint32_t)p.N_h * (uint32_t)p.NLP;
+    const uint32_t stride = gridDim.x * blockDim.x * U;
+    for (uint32_t s0 = (blockIdx.x * blockDim.x + threadIdx.x) * U; s0 < total; s0 += stride) {
+        float u[U], v[U];
+        uint32_t b[U];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) v[e] = s_acc[priv_index(pxi, c + e, p.C_h, p.swizzle)];
-            if (v[0] != 0.0f || v[1] != 0.0f || v[2] != 0.0f || v[3] != 0.0f) {
-                int l = 0;
-                while (!(lt.priv[l] >= 0 && pxi >= lt.priv[l] && pxi < lt.priv[l] + lt.W[l] * lt.H[l])) ++l;
-                const int gpix = lt.start[l] + (pxi - lt.priv[l]);
-                red_add_v4(gb + (int64_t)gpix * sP + c, v[0], v[1], v[2], v[3]);
+        for (int t = 0; t < U; ++t) {
+            const uint32_t s = s0 + t;
+            u[t] = v[t] = 0.0f;
+            b[t] = 0;
+            if (s < total) {
+                b[t] = s / per_batch;
+                const float *lp = loc + b[t] * p.l_sB + (int64_t)(s - b[t] * per_batch) * p.l_sJ;
+                u[t] = __ldg(lp);
+                v[t] = __ldg(lp + p.l_sXY);
             }
+        }
+#pragma unroll
+        for (int t = 0; t < U; ++t) {
+            const uint32_t s = s0 + t;
+            if (s < total) {
+                const uint32_t rowq = p.div_nlp.div(s);  // (b * N_q + q) * N_h + h
+                const uint32_t j = s - rowq * (uint32_t)p.NLP;
+                const uint32_t h = rowq - p.div_h.div(rowq) * (uint32_t)p.N_h;
+                const int l = (int)p.div_p.div(j);
+                const int W = lt.W[l], H = lt.H[l];
+                const Cell c = make_cell<PAD>(u[t], v[t], lt.sx[l], lt.sy[l], p.off, W, H, p.padding);
+                const int key = cell_key(c, W, lt.kst[l]);
+                if (key >= 0)
+                    atomicAdd(counts + (b[t] * (uint32_t)p.N_h + h) * (uint32_t)p.K_bh + (uint32_t)key, 1);
+            }
+        }
+    }
+}
+
+// Exclusive prefix sum of n counts, in tiles of kScanTile: pass 1 sums each
+// tile, pass 2 scans each tile after the sums of the tiles before it, in
+// place (counts become offsets), copies the offsets to cursor and writes the
+// grand total to offsets[n].
+constexpr int kScanThreads = 1024;
+constexpr int kScanPer = 4;
+constexpr int kScanTile = kScanThreads * kScanPer;
+
+__global__ void msda_scan_tiles_kernel(const int *__restrict__ counts, uint32_t n, int *__restrict__ tile_sums);
+__global__ void msda_scan_apply_kernel(int *__restrict__ offsets, uint32_t n, const int *__restrict__ tile_sums,
+                                       int *__restrict__ cursor);
+
+// One group of G lanes per cell key, keys taken level by level in the order
+// p.ilev (levels with the fewest pixels, hence the longest lists, first).  The
+// group walks the key's list: every lane loads the entry (row, A, fx, fy),
+// forms the four corner weights A(1-fx)(1-fy), A fx(1-fy), A(1-fx)fy, A fx fy
+// and adds weight * (its chunks of grad_output's row) into four per-corner
+// sums; then it adds each sum whose corner lies in the map into the
+// accumulator (red.global.add.v4.f32).
+template <typename T, int VEC, int G, int NCH>
+__global__ void __launch_bounds__(256, 3)
+msda_gv_reduce_kernel(const __grid_constant__ Params p, const T *__restrict__ grad_out,
+                      const int *__restrict__ offsets, const uint4 *__restrict__ entries,
+                      float *__restrict__ gv_acc) {
+    constexpr int GPB = 256 / G;
+    const int lane = threadIdx.x & 31;
+    const int r = lane & (G - 1);
+    const uint32_t item = blockIdx.x * GPB + threadIdx.x / G;
+    if (item >= p.nkeys) return;  // the whole group leaves together
+    int pos = 0;
+    while (item >= p.iend[pos]) ++pos;
+    const int l = p.ilev[pos];
+    const uint32_t rel = item - (pos ? p.iend[pos - 1] : 0u);
+    const int W = p.W[l], H = p.H[l];
+    const uint32_t KL = (uint32_t)(H + 1) * (uint32_t)(W + 1);
+    const uint32_t bh = rel / KL;
+    const int cl = (int)(rel - bh * KL);
+    const int y0 = cl / (W + 1) - 1, x0 = cl % (W + 1) - 1;
+    const uint32_t gkey = bh * (uint32_t)p.K_bh + (uint32_t)p.kst[l] + (uint32_t)cl;
+    const int beg = offsets[gkey], end = offsets[gkey + 1];
+    if (beg >= end) return;
+    int nk = 0;
+#pragma unroll
+    for (int k = 0; k < NCH; ++k) nk += (k * G + r < p.chunks);
+
+    float acc[4][NCH][VEC];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int k = 0; k < NCH; ++k)
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) acc[i][k][e] = 0.0f;
+    const T *gbase = grad_out + r * VEC;
+    constexpr int U = 8;  // entries in flight
+    for (int e0 = beg; e0 < end; e0 += U) {
+        uint4 ent[U];
+        float gv[U][NCH][VEC];
+#pragma unroll
+        for (int t = 0; t < U; ++t) {
+            ent[t] = e0 + t < end ? __ldg(entries + e0 + t) : make_uint4(0u, 0u, 0u, 0u);
+            const uint32_t row = ent[t].x < p.rows ? ent[t].x : 0u;  // an entry's row is always < rows
+#pragma unroll
+            for (int k = 0; k < NCH; ++k)
+                if (k < nk) VecIO<T, VEC>::load(gbase + (int64_t)row * p.C_h + k * G * VEC, gv[t][k]);
+        }
+#pragma unroll
+        for (int t = 0; t < U; ++t) {
+            const float A = __uint_as_float(ent[t].y), fx = __uint_as_float(ent[t].z),
+                        fy = __uint_as_float(ent[t].w);
+            const float A1 = A * fx;
+            const float ax0 = A - A1, ax1 = A1, ay0 = 1.0f - fy, ay1 = fy;
+            const float w[4] = {ay0 * ax0, ay0 * ax1, ay1 * ax0, ay1 * ax1};
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int k = 0; k < NCH; ++k)
+                    if (k < nk)
+#pragma unroll
+                        for (int e = 0; e < VEC; ++e) acc[i][k][e] = fmaf(w[i], gv[t][k][e], acc[i][k][e]);
+        }
+    }
+    const uint32_t b = p.div_h.div(bh), h = bh - b * (uint32_t)p.N_h;
+    float *gb = gv_acc + b * p.v_sB + (int64_t)h * p.v_sH + r * VEC;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int y = y0 + (i >> 1), x = x0 + (i & 1);
+        if ((unsigned)y < (unsigned)H && (unsigned)x < (unsigned)W) {
+            float *dst = gb + (int64_t)(p.start[l] + y * W + x) * p.v_sP;
+#pragma unroll
+            for (int k = 0; k < NCH; ++k)
+                if (k < nk) RedIO<VEC>::add(dst + k * G * VEC, acc[i][k], 1.0f);
         }
     }
 }
@@ -721,25 +854,34 @@ inline cudaError_t launch_forward(const Params &p, bool vec, int G, int NCH, con
     return vec ? launch_forward_path<T, true>(p, G, NCH, value, loc, attn, out, stream)
                : launch_forward_path<T, false>(p, G, NCH, value, loc, attn, out, stream);
 }
+
+// Buffers of the backward: the binary32 grad_value accumulator and, for the
+// cell-sorted grad_value, the key counts / offsets (nkeys + 1), the cursors
+// (nkeys), the tile sums of the scan and the entries (capacity).
+struct BwdBuffers {
+    float *gv_acc;
+    float *grad_loc, *grad_attn;
+    int *offsets, *cursor, *tile_sums;
+    uint4 *entries;
+};
 template <typename T, int PAD>
-cudaError_t launch_backward_pad(const Params &p, int G, int NCH, bool priv, const T *grad_out, const T *value,
-                                const float *loc, const float *attn, float *gv_acc, float *grad_loc,
-                                float *grad_attn, cudaStream_t stream);
+cudaError_t launch_backward_pad(const Params &p, int G, int NCH, bool sort, const T *grad_out, const T *value,
+                                const float *loc, const float *attn, const BwdBuffers &bb, cudaStream_t stream);
 // Dispatch on vector path / padding to the launch_backward_pad instantiations.
 template <typename T>
-inline cudaError_t launch_backward(const Params &p, bool vec, int G, int NCH, bool priv, const T *grad_out,
-                                   const T *value, const float *loc, const float *attn, float *gv_acc,
-                                   float *grad_loc, float *grad_attn, cudaStream_t stream) {
+inline cudaError_t launch_backward(const Params &p, bool vec, int G, int NCH, bool sort, const T *grad_out,
+                                   const T *value, const float *loc, const float *attn, const BwdBuffers &bb,
+                                   cudaStream_t stream) {
     if (p.rows == 0) return cudaSuccess;
-    if (!vec)
-        return launch_backward_pad<T, -1>(p, G, NCH, false, grad_out, value, loc, attn, gv_acc, grad_loc,
-                                          grad_attn, stream);
-    if (p.padding == 0)
-        return launch_backward_pad<T, 0>(p, G, NCH, priv, grad_out, value, loc, attn, gv_acc, grad_loc,
-                                         grad_attn, stream);
-    return launch_backward_pad<T, 1>(p, G, NCH, priv, grad_out, value, loc, attn, gv_acc, grad_loc, grad_attn,
-                                     stream);
+    if (!vec) return launch_backward_pad<T, -1>(p, G, NCH, sort, grad_out, value, loc, attn, bb, stream);
+    if (p.padding == 0) return launch_backward_pad<T, 0>(p, G, NCH, sort, grad_out, value, loc, attn, bb, stream);
+    return launch_backward_pad<T, 1>(p, G, NCH, sort, grad_out, value, loc, attn, bb, stream);
 }
+// Cell-sorted grad_value, steps 1-2 (count, scan) and 4 (reduce).
+cudaError_t launch_sort_keys(const Params &p, const float *loc, const BwdBuffers &bb, cudaStream_t stream);
+template <typename T, bool VECTOR>
+cudaError_t launch_gv_reduce(const Params &p, int G, int NCH, const T *grad_out, const BwdBuffers &bb,
+                             cudaStream_t stream);
 cudaError_t launch_zero_f32(float *p, int64_t n, cudaStream_t stream);
 cudaError_t launch_f32_to_bf16(const float *acc, __nv_bfloat16 *out, int64_t n, cudaStream_t stream);
 

@@ -1,17 +1,12 @@
 // msda_launch.cuh -- host-side launchers: pick the kernel instantiation for
 // (vector width, lanes per row G, channel chunks per lane NCH, padding,
-// backward outputs).
+// backward outputs, grad_value path) and size the grids.
 #pragma once
 
 #include "msda_kernels.cuh"
 #include "msda_shape.cuh"
 
 namespace msda {
-
-inline unsigned grid_for(uint32_t rows, int G) {
-    const uint64_t threads = (uint64_t)rows * (uint64_t)G;
-    return (unsigned)((threads + kThreads - 1) / kThreads);
-}
 
 #define MSDA_SHAPES(X)                                                                            \
     X(1, 1) X(2, 1) X(2, 2) X(2, 4) X(2, 8) X(4, 1) X(4, 2) X(4, 4) X(4, 8) X(8, 1) X(8, 2) X(8, 4) \
@@ -25,14 +20,24 @@ int resident_blocks(K kernel, int threads, size_t smem) {
     return n;
 }
 
-// The forward's blocks loop over rows: launch no more than fit at once.
+// Row kernels (one group of G lanes per row): as many blocks as fit on the GPU
+// at once (fewer when the rows do not fill them); the blocks sweep the rows
+// with a grid stride.
+template <typename K>
+unsigned row_grid(K kernel, int G, const Params &p) {
+    const unsigned gpb = kThreads / G;  // rows a block works on at once
+    uint64_t blocks = ((uint64_t)p.rows + gpb - 1) / gpb;
+    const int per_sm = resident_blocks(kernel, kThreads, 0);
+    if (per_sm > 0 && p.n_sm > 0 && (uint64_t)per_sm * p.n_sm < blocks) blocks = (uint64_t)per_sm * p.n_sm;
+    if (blocks < 1) blocks = 1;
+    return (unsigned)blocks;
+}
+
 template <typename T, int V, int GG, int NN, int PAD>
 cudaError_t fwd_launch(const Params &p, const T *value, const float *loc, const float *attn, T *out,
                        cudaStream_t stream) {
     auto kernel = msda_forward_kernel<T, V, GG, NN, PAD>;
-    unsigned blocks = grid_for(p.rows, GG);
-    const int per_sm = resident_blocks(kernel, kThreads, 0);
-    if (per_sm > 0 && p.n_sm > 0 && (uint64_t)per_sm * p.n_sm < blocks) blocks = (unsigned)(per_sm * p.n_sm);
+    const unsigned blocks = row_grid(kernel, GG, p);
     kernel<<<blocks, kThreads, 0, stream>>>(p, value, loc, attn, out);
     return cudaGetLastError();
 }
@@ -63,42 +68,33 @@ cudaError_t launch_forward_path(const Params &p, int G, int NCH, const T *value,
     return cudaErrorInvalidConfiguration;
 }
 
-template <typename T, int V, int GG, int NN, int PAD, int FL, bool PRIV>
+template <typename T, int V, int GG, int NN, int PAD, int FL, bool SORT>
 cudaError_t bwd_launch(const Params &p, const T *grad_out, const T *value, const float *loc, const float *attn,
-                       float *gv_acc, float *grad_loc, float *grad_attn, cudaStream_t stream) {
-    const dim3 grid((unsigned)(p.rows / (uint32_t)p.N_q), (unsigned)((p.N_q + p.q_chunk - 1) / p.q_chunk));
-    const dim3 block(kBwdThreads);
-    size_t smem = 0;
-    auto kernel = msda_backward_kernel<T, V, GG, NN, PAD, FL, PRIV>;
-    if constexpr (PRIV) {
-        smem = (size_t)p.priv_pixels * (size_t)p.C_h * sizeof(float);
-        const cudaError_t e =
-            cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-    }
-    kernel<<<grid, block, smem, stream>>>(p, grad_out, value, loc, attn, gv_acc, grad_loc, grad_attn);
+                       const BwdBuffers &bb, cudaStream_t stream) {
+    auto kernel = msda_backward_kernel<T, V, GG, NN, PAD, FL, SORT>;
+    const unsigned blocks = row_grid(kernel, GG, p);
+    kernel<<<blocks, kThreads, 0, stream>>>(p, grad_out, value, loc, attn, bb.gv_acc, bb.grad_loc, bb.grad_attn,
+                                            bb.cursor, bb.entries);
     return cudaGetLastError();
 }
 
 template <typename T, int V, int GG, int NN, int PAD>
-cudaError_t bwd_flags(const Params &p, bool priv, const T *grad_out, const T *value, const float *loc,
-                      const float *attn, float *gv_acc, float *grad_loc, float *grad_attn, cudaStream_t stream) {
+cudaError_t bwd_flags(const Params &p, bool sort, const T *grad_out, const T *value, const float *loc,
+                      const float *attn, const BwdBuffers &bb, cudaStream_t stream) {
     constexpr int ALL = kGradValue | kGradLoc | kGradAttn;
-#define MSDA_BWD(FL, PR) \
-    return bwd_launch<T, V, GG, NN, PAD, FL, PR>(p, grad_out, value, loc, attn, gv_acc, grad_loc, grad_attn, stream)
+#define MSDA_BWD(FL, SO) return bwd_launch<T, V, GG, NN, PAD, FL, SO>(p, grad_out, value, loc, attn, bb, stream)
     if constexpr (PAD < 0 || !specialised_shape(GG, NN)) {
+        if (sort) MSDA_BWD(-1, true);
         MSDA_BWD(-1, false);
     } else {
-        if constexpr (GG <= 8) {
-            if (priv) {
-                if (p.flags == ALL) MSDA_BWD(ALL, true);
-                if (p.flags == kGradValue) MSDA_BWD(kGradValue, true);
-                MSDA_BWD(-1, true);
-            }
+        if (!(p.flags & kGradValue)) MSDA_BWD(kGradLoc | kGradAttn, false);
+        if (sort) {
+            if (p.flags == ALL) MSDA_BWD(ALL, true);
+            if (p.flags == kGradValue) MSDA_BWD(kGradValue, true);
+            MSDA_BWD(-1, true);
         }
         if (p.flags == ALL) MSDA_BWD(ALL, false);
         if (p.flags == kGradValue) MSDA_BWD(kGradValue, false);
-        if (!(p.flags & kGradValue)) MSDA_BWD(kGradLoc | kGradAttn, false);
         MSDA_BWD(-1, false);
     }
 #undef MSDA_BWD
@@ -111,26 +107,44 @@ cudaError_t bwd_flags(const Params &p, bool priv, const T *grad_out, const T *va
 //   PAD -2   : vector path, wide shapes, padding and outputs read at run time;
 //   PAD -1   : scalar path (unaligned pointers or C_h not a multiple of 4).
 template <typename T, int PAD>
-cudaError_t launch_backward_pad(const Params &p, int G, int NCH, bool priv, const T *grad_out, const T *value,
-                                const float *loc, const float *attn, float *gv_acc, float *grad_loc,
-                                float *grad_attn, cudaStream_t stream) {
+cudaError_t launch_backward_pad(const Params &p, int G, int NCH, bool sort, const T *grad_out, const T *value,
+                                const float *loc, const float *attn, const BwdBuffers &bb, cudaStream_t stream) {
     constexpr int V = PAD == -1 ? 1 : BwdVecWidth<T>::value;
 #define MSDA_BWD_CASE(GG, NN)                                                                     \
     if constexpr (reachable(GG, NN, MSDA_BWD_LANES)) {                                            \
         if (G == GG && NCH == NN) {                                                               \
             if constexpr (PAD == -1 || (PAD == -2) != specialised_shape(GG, NN))                  \
-                return bwd_flags<T, V, GG, NN, PAD>(p, PAD < 0 ? false : priv, grad_out, value,   \
-                                                    loc, attn, gv_acc, grad_loc, grad_attn,       \
-                                                    stream);                                      \
+                return bwd_flags<T, V, GG, NN, PAD>(p, sort, grad_out, value, loc, attn, bb, stream); \
             else if constexpr (PAD >= 0)                                                          \
-                return launch_backward_pad<T, -2>(p, G, NCH, false, grad_out, value, loc, attn,   \
-                                                  gv_acc, grad_loc, grad_attn, stream);           \
+                return launch_backward_pad<T, -2>(p, G, NCH, sort, grad_out, value, loc, attn, bb, \
+                                                  stream);                                        \
             else                                                                                  \
                 return cudaErrorInvalidConfiguration;                                             \
         }                                                                                         \
     }
     MSDA_SHAPES(MSDA_BWD_CASE)
 #undef MSDA_BWD_CASE
+    return cudaErrorInvalidConfiguration;
+}
+
+// Cell-sorted grad_value, step 4: one group per key.
+template <typename T, bool VECTOR>
+cudaError_t launch_gv_reduce(const Params &p, int G, int NCH, const T *grad_out, const BwdBuffers &bb,
+                             cudaStream_t stream) {
+    if (p.nkeys == 0) return cudaSuccess;
+    constexpr int V = VECTOR ? BwdVecWidth<T>::value : 1;
+#define MSDA_RED_CASE(GG, NN)                                                                     \
+    if constexpr (reachable(GG, NN, MSDA_BWD_LANES)) {                                            \
+        if (G == GG && NCH == NN) {                                                               \
+            constexpr unsigned gpb = 256 / GG;                                                    \
+            const unsigned blocks = (unsigned)((p.nkeys + gpb - 1) / gpb);                        \
+            msda_gv_reduce_kernel<T, V, GG, NN><<<blocks, 256, 0, stream>>>(p, grad_out, bb.offsets, \
+                                                                          bb.entries, bb.gv_acc); \
+            return cudaGetLastError();                                                            \
+        }                                                                                         \
+    }
+    MSDA_SHAPES(MSDA_RED_CASE)
+#undef MSDA_RED_CASE
     return cudaErrorInvalidConfiguration;
 }
 

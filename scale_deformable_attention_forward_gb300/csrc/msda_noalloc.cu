@@ -23,6 +23,7 @@
 // overlaps on the GPU (different streams, or different host threads without
 // ordering) race on the array and give wrong grad_value.
 #include "msda.h"
+#include "msda_entry.h"
 
 #include <cuda_runtime.h>
 
@@ -83,16 +84,19 @@ extern "C" int msda_backward_noalloc(const msda_desc *desc, const void *grad_out
         }
         if (elems * sizeof(float) > kScratchBytes) return MSDA_ERR_WORKSPACE;
     }
-    const size_t need = msda_backward_workspace_size(desc, compute_grad_value);
+    // grad_value goes straight into the accumulator with atomics here: the
+    // cell-sorted path's buffers grow with the number of samples.
+    const size_t need = msda::backward_workspace_bytes(desc, compute_grad_value, false);
     if (need > kScratchBytes) return MSDA_ERR_WORKSPACE;
     void *ws = nullptr;
     if (need > 0) {
         const int rc = scratch_address(&ws);
         if (rc != MSDA_OK) return rc;
     }
-    // msda_backward validates every argument, zeroes the part of the
+    // The backward validates every argument, zeroes the part of the
     // accumulator it uses and enqueues the kernels on `stream`.
-    return msda_backward(desc, grad_output, value, sampling_locations, attention_weights, compute_grad_value,
-                         compute_grad_sampling_locations, compute_grad_attention_weights, grad_value,
-                         grad_sampling_locations, grad_attention_weights, ws, need, stream);
+    return msda::backward_entry(desc, grad_output, value, sampling_locations, attention_weights,
+                                compute_grad_value, compute_grad_sampling_locations,
+                                compute_grad_attention_weights, grad_value, grad_sampling_locations,
+                                grad_attention_weights, ws, need, false, stream);
 }

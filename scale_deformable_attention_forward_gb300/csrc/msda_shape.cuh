@@ -17,12 +17,14 @@
 
 namespace msda {
 
-// Elements per lane access.  Forward: 16-byte loads.  Backward: 4 channels
-// per lane for both dtypes, so that one red.global.add.v4.f32 per lane makes
-// a group's atomics cover whole 128-byte lines of the binary32 accumulator.
-template <typename T> struct VecWidth;
-template <> struct VecWidth<float> { static constexpr int value = 4; };
-template <> struct VecWidth<__nv_bfloat16> { static constexpr int value = 8; };
+// Elements per lane access: 4 channels per lane for both dtypes.  A group of
+// 8 lanes then covers a 32-channel corner row with one load instruction (L1
+// resolves about one distinct 128-byte line per clock whatever part of it an
+// instruction reads, so 8-byte bfloat16 loads cost what 16-byte ones do), the
+// forward sums the groups' partial outputs over few shuffles, and in the
+// backward one red.global.add.v4.f32 per lane makes a group's atomics cover
+// whole 128-byte lines of the binary32 accumulator.
+template <typename T> struct VecWidth { static constexpr int value = 4; };
 template <typename T> struct BwdVecWidth { static constexpr int value = 4; };
 
 constexpr int pow2ceil(int x) {

@@ -70,6 +70,34 @@ def test_channel_counts(dtype, C_h):
     check_workload(w, flag_sets=[(True, True, True)])
 
 
+# The cell-sorted grad_value (count, scan, append, per-cell reduction) runs
+# when a problem has at least two samples per cell key; the problems above are
+# sparser and take the direct-atomic grad_value.  These repeat the option
+# matrix and the channel counts on problems dense enough for the sorted path.
+def _dense(w):
+    keys = w.B * w.N_h * sum((h + 1) * (wd + 1) for h, wd in w.levels)
+    samples = w.B * w.n_queries * w.N_h * w.N_l * w.N_p
+    assert samples >= 2 * keys, "not dense enough for the cell-sorted grad_value"
+    return w
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("vl", ["BLNC", "BNLC"])
+@pytest.mark.parametrize("ll", ["BQHLP2", "B2QHLP"])
+@pytest.mark.parametrize("align", [False, True])
+@pytest.mark.parametrize("pad", ["zeros", "border"])
+def test_option_matrix_sorted(dtype, vl, ll, align, pad):
+    w = _dense(_small(dtype, vl, ll, align, pad, N_q=150, seed=13))
+    check_workload(w, flag_sets=[(True, True, True), (True, False, False)], check_forward=False)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("C_h", [1, 3, 4, 5, 8, 12, 40, 96, 256])
+def test_channel_counts_sorted(dtype, C_h):
+    w = _dense(_small(dtype, "BLNC", "BQHLP2", False, "zeros", C_h=C_h, N_q=120, N_h=2, N_p=2, seed=C_h + 100))
+    check_workload(w, flag_sets=[(True, False, False)], check_forward=False)
+
+
 @pytest.mark.parametrize("N_p", [1, 5, 8, 13])
 def test_points_per_level(N_p):
     """N_l*N_p not a multiple of the samples in flight per warp."""
