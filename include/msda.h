@@ -175,6 +175,55 @@ int msda_backward(const msda_desc *desc, const void *grad_output, const void *va
                   void *grad_sampling_locations, void *grad_attention_weights, void *workspace,
                   size_t workspace_bytes, cudaStream_t stream);
 
+/* Accumulating backward ("MS Deformable Attention Backward Kernel API
+ * Reference", Parameters: grad_value_buffers_in, prev_reduced_grad_value,
+ * dump_reduced_grad_value).  The pages let a call add into persistent
+ * grad_value buffers instead of zeroing them, so that calls over query chunks
+ * or over several micro-batches build one total.  Here that state is one
+ * caller-owned binary32 buffer:
+ *   grad_value_accum    binary32, value's shape and layout, 4-byte aligned
+ *                       (16-byte for the vector path); this call's grad_value
+ *                       is ADDED to it (read-modify-write, never zeroed, never
+ *                       rounded to value_dtype, also for BF16 value).
+ * Every other argument is as in msda_backward (the workspace size is
+ * msda_backward_workspace_size's; the accumulator part of it is not used).
+ * grad_sampling_locations and grad_attention_weights are overwritten as in
+ * msda_backward.  After the call grad_value_accum = its previous contents +
+ * this call's grad_value, up to binary32 rounding in an unspecified order
+ * (atomic adds).  Calls that overlap on the GPU may add into the same
+ * accumulator.  Returns MSDA_OK or a negative msda_status; a failed call
+ * leaves the accumulator untouched. */
+int msda_backward_accumulate(const msda_desc *desc, const void *grad_output, const void *value,
+                             const void *sampling_locations, const void *attention_weights,
+                             int compute_grad_value, int compute_grad_sampling_locations,
+                             int compute_grad_attention_weights, float *grad_value_accum,
+                             void *grad_sampling_locations, void *grad_attention_weights, void *workspace,
+                             size_t workspace_bytes, cudaStream_t stream);
+
+/* Forward and backward with attention LOGITS.  The pages take attention
+ * weights as an input ("MS Deformable Attention Kernel API Reference",
+ * Parameters: attention_weights); models produce them as a softmax over the
+ * N_l*N_p (level, point) slots of each (b, q, h) (the workloads here are built
+ * that way).  These entry points fuse that producer: attention_logits has
+ * attention_weights' shape and dtype, and for every (b, q, h)
+ *     A[l, p] = exp(z[l, p] - m) / sum_{l', p'} exp(z[l', p'] - m),
+ *     m = max z over the row,
+ * then the operation is msda_forward / msda_backward with those weights.
+ * msda_backward_logits returns in grad_attention_logits the gradient with
+ * respect to the logits,
+ *     dz[l, p] = A[l, p] * (gA[l, p] - sum_{l', p'} A[l', p'] gA[l', p']),
+ * gA being the attention-weight gradient; attention_logits is read for every
+ * output flag.  All other arguments, results, ownership and errors are those
+ * of msda_forward / msda_backward (same workspace size). */
+int msda_forward_logits(const msda_desc *desc, const void *value, const void *sampling_locations,
+                        const void *attention_logits, void *out, cudaStream_t stream);
+int msda_backward_logits(const msda_desc *desc, const void *grad_output, const void *value,
+                         const void *sampling_locations, const void *attention_logits,
+                         int compute_grad_value, int compute_grad_sampling_locations,
+                         int compute_grad_attention_logits, void *grad_value, void *grad_sampling_locations,
+                         void *grad_attention_logits, void *workspace, size_t workspace_bytes,
+                         cudaStream_t stream);
+
 /* Size of the library-owned scratch array used by msda_backward_noalloc:
  * 32 MiB, i.e. room for a binary32 accumulator of B*L*N_h*C_h <= 8,388,608
  * elements (one 4-level Deformable-DETR pyramid image with 8 heads of 32

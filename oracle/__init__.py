@@ -142,6 +142,46 @@ class Oracle:
         return gv, gl, ga
 
 
+def softmax_rows(attention_logits) -> np.ndarray:
+    """Attention weights from logits (B, N_q, N_h, N_l, N_p): the softmax over
+    the N_l*N_p (level, point) slots of each (b, q, h), in float64 -- how the
+    workloads build their weights from N(0,1) logits."""
+    z = _f64(attention_logits)
+    flat = z.reshape(z.shape[:3] + (-1,))
+    e = np.exp(flat - flat.max(axis=-1, keepdims=True))
+    return (e / e.sum(axis=-1, keepdims=True)).reshape(z.shape)
+
+
+def _forward_logits(self, value, spatial_shapes, level_start_index, sampling_locations, attention_logits,
+                    **kw) -> np.ndarray:
+    """The forward with the weights softmax(logits) (see softmax_rows)."""
+    return self.forward(value, spatial_shapes, level_start_index, sampling_locations,
+                        softmax_rows(attention_logits), **kw)
+
+
+def _backward_logits(self, grad_output, value, spatial_shapes, level_start_index, sampling_locations,
+                     attention_logits, compute_grad_value: bool = True,
+                     compute_grad_sampling_locations: bool = True, compute_grad_attention_logits: bool = True,
+                     **kw):
+    """The backward with the weights softmax(logits): grad_value and
+    grad_sampling_locations as for those weights, and for the logits the
+    chain rule of the softmax, dz = A * (gA - sum over the row of A * gA)."""
+    A = softmax_rows(attention_logits)
+    gv, gl, gA = self.backward(grad_output, value, spatial_shapes, level_start_index, sampling_locations, A,
+                               compute_grad_value=compute_grad_value,
+                               compute_grad_sampling_locations=compute_grad_sampling_locations,
+                               compute_grad_attention_weights=compute_grad_attention_logits, **kw)
+    gz = None
+    if compute_grad_attention_logits:
+        s = (A * gA).reshape(A.shape[:3] + (-1,)).sum(axis=-1)[..., None, None]
+        gz = A * (gA - s)
+    return gv, gl, gz
+
+
+Oracle.forward_logits = _forward_logits
+Oracle.backward_logits = _backward_logits
+
+
 def default() -> Oracle:
     """The oracle built from ``msda_oracle.c`` (compiled on first use)."""
     global _default
@@ -159,3 +199,13 @@ def forward(*args, **kwargs) -> np.ndarray:
 def backward(*args, **kwargs):
     """MSDA backward in float64 (see :meth:`Oracle.backward`)."""
     return default().backward(*args, **kwargs)
+
+
+def forward_logits(*args, **kwargs) -> np.ndarray:
+    """MSDA forward with attention logits (see :func:`softmax_rows`)."""
+    return default().forward_logits(*args, **kwargs)
+
+
+def backward_logits(*args, **kwargs):
+    """MSDA backward with attention logits; returns the logits' gradient third."""
+    return default().backward_logits(*args, **kwargs)

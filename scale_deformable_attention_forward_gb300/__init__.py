@@ -81,6 +81,12 @@ def load_library() -> ctypes.CDLL:
             lib.msda_backward_workspace_size.restype = Z
             lib.msda_backward.argtypes = [D, P, P, P, P, I, I, I, P, P, P, P, Z, P]
             lib.msda_backward.restype = I
+            lib.msda_backward_accumulate.argtypes = [D, P, P, P, P, I, I, I, P, P, P, P, Z, P]
+            lib.msda_backward_accumulate.restype = I
+            lib.msda_forward_logits.argtypes = [D, P, P, P, P, P]
+            lib.msda_forward_logits.restype = I
+            lib.msda_backward_logits.argtypes = [D, P, P, P, P, I, I, I, P, P, P, P, Z, P]
+            lib.msda_backward_logits.restype = I
             lib.msda_status_string.argtypes = [I]
             lib.msda_status_string.restype = ctypes.c_char_p
             lib.msda_last_cuda_error.argtypes = []
@@ -199,7 +205,7 @@ def _stream(device):
 
 def msda_forward(value, spatial_shapes, level_start_index, sampling_locations, attention_weights,
                  value_layout: str = "BLNC", sampling_locations_layout: str = "BQHLP2",
-                 align_corners: bool = False, padding_mode: str = "zeros", out=None):
+                 align_corners: bool = False, padding_mode: str = "zeros", out=None, _logits: bool = False):
     """Multi-scale deformable attention forward on the GPU.
 
     value (B,L,N_h,C_h) or (B,N_h,L,C_h), float32 or bfloat16;
@@ -228,12 +234,22 @@ def msda_forward(value, spatial_shapes, level_start_index, sampling_locations, a
         _check(out, "out", value.dtype, (B, N_q, N_h * C_h), dev)
     d = make_desc((B, N_q, N_h, C_h, N_l, N_p, L), shapes, starts, value_layout,
                   sampling_locations_layout, align_corners, padding_mode, vdt)
+    fn, name = (lib.msda_forward_logits, "msda_forward_logits") if _logits else (lib.msda_forward, "msda_forward")
     with torch.cuda.device(dev):
-        rc = lib.msda_forward(d.ref(), _ptr(value), _ptr(sampling_locations), _ptr(attention_weights),
-                              _ptr(out), _stream(dev))
+        rc = fn(d.ref(), _ptr(value), _ptr(sampling_locations), _ptr(attention_weights), _ptr(out), _stream(dev))
     if rc != 0:
-        raise MSDAError(rc, "msda_forward")
+        raise MSDAError(rc, name)
     return out
+
+
+def msda_forward_logits(value, spatial_shapes, level_start_index, sampling_locations, attention_logits,
+                        value_layout: str = "BLNC", sampling_locations_layout: str = "BQHLP2",
+                        align_corners: bool = False, padding_mode: str = "zeros", out=None):
+    """msda_forward with attention logits (B,N_q,N_h,N_l,N_p), float32: the
+    weights are the softmax over each (b, q, h)'s N_l*N_p logits, computed in
+    the kernel."""
+    return msda_forward(value, spatial_shapes, level_start_index, sampling_locations, attention_logits,
+                        value_layout, sampling_locations_layout, align_corners, padding_mode, out, _logits=True)
 
 
 def msda_backward_workspace_size(value, spatial_shapes, level_start_index, sampling_locations,
@@ -252,7 +268,7 @@ def msda_backward(grad_output, value, spatial_shapes, level_start_index, samplin
                   align_corners: bool = False, padding_mode: str = "zeros", compute_grad_value: bool = True,
                   compute_grad_sampling_locations: bool = True, compute_grad_attention_weights: bool = True,
                   grad_value=None, grad_sampling_locations=None, grad_attention_weights=None,
-                  workspace=None) -> Tuple:
+                  workspace=None, _accumulate: bool = False, _logits: bool = False) -> Tuple:
     """Multi-scale deformable attention backward on the GPU.
 
     Returns (grad_value, grad_sampling_locations, grad_attention_weights);
@@ -283,9 +299,14 @@ def msda_backward(grad_output, value, spatial_shapes, level_start_index, samplin
         raise ValueError("at least one of compute_grad_value / compute_grad_sampling_locations / "
                          "compute_grad_attention_weights must be True")
     if fv:
-        if grad_value is None:
-            grad_value = torch.empty_like(value)
-        _check(grad_value, "grad_value", value.dtype, value.shape, dev)
+        if _accumulate:
+            if grad_value is None:
+                raise ValueError("msda_backward_accumulate needs grad_value_accum")
+            _check(grad_value, "grad_value_accum", torch.float32, value.shape, dev)
+        else:
+            if grad_value is None:
+                grad_value = torch.empty_like(value)
+            _check(grad_value, "grad_value", value.dtype, value.shape, dev)
     else:
         grad_value = None
     if fl:
@@ -309,10 +330,47 @@ def msda_backward(grad_output, value, spatial_shapes, level_start_index, samplin
         elif workspace.device != dev or workspace.numel() * workspace.element_size() < ws_bytes:
             raise ValueError(f"workspace must hold {ws_bytes} bytes on {dev}")
     with torch.cuda.device(dev):
-        rc = lib.msda_backward(d.ref(), _ptr(grad_output), _ptr(value), _ptr(sampling_locations),
+        fn = (lib.msda_backward_accumulate if _accumulate else
+              lib.msda_backward_logits if _logits else lib.msda_backward)
+        rc = fn(d.ref(), _ptr(grad_output), _ptr(value), _ptr(sampling_locations),
                                _ptr(attention_weights), int(fv), int(fl), int(fa), _ptr(grad_value),
                                _ptr(grad_sampling_locations), _ptr(grad_attention_weights),
                                _ptr(workspace) if ws_bytes > 0 else None, ws_bytes, _stream(dev))
     if rc != 0:
-        raise MSDAError(rc, "msda_backward")
+        raise MSDAError(rc, "msda_backward_accumulate" if _accumulate else
+                        "msda_backward_logits" if _logits else "msda_backward")
     return grad_value, grad_sampling_locations, grad_attention_weights
+
+
+
+def msda_backward_accumulate(grad_output, value, spatial_shapes, level_start_index, sampling_locations,
+                             attention_weights, grad_value_accum, value_layout: str = "BLNC",
+                             sampling_locations_layout: str = "BQHLP2", align_corners: bool = False,
+                             padding_mode: str = "zeros", compute_grad_value: bool = True,
+                             compute_grad_sampling_locations: bool = True,
+                             compute_grad_attention_weights: bool = True, grad_sampling_locations=None,
+                             grad_attention_weights=None, workspace=None) -> Tuple:
+    """msda_backward that ADDS this call's grad_value into ``grad_value_accum``
+    (a float32 tensor of value's shape and layout, never zeroed by the call),
+    for query-chunked calls or gradient accumulation over micro-batches.
+    Returns (grad_value_accum, grad_sampling_locations, grad_attention_weights)."""
+    return msda_backward(grad_output, value, spatial_shapes, level_start_index, sampling_locations,
+                         attention_weights, value_layout, sampling_locations_layout, align_corners, padding_mode,
+                         compute_grad_value, compute_grad_sampling_locations, compute_grad_attention_weights,
+                         grad_value=grad_value_accum, grad_sampling_locations=grad_sampling_locations,
+                         grad_attention_weights=grad_attention_weights, workspace=workspace, _accumulate=True)
+
+
+def msda_backward_logits(grad_output, value, spatial_shapes, level_start_index, sampling_locations,
+                         attention_logits, value_layout: str = "BLNC", sampling_locations_layout: str = "BQHLP2",
+                         align_corners: bool = False, padding_mode: str = "zeros", compute_grad_value: bool = True,
+                         compute_grad_sampling_locations: bool = True, compute_grad_attention_logits: bool = True,
+                         grad_value=None, grad_sampling_locations=None, grad_attention_logits=None,
+                         workspace=None) -> Tuple:
+    """msda_backward with attention logits (see msda_forward_logits).
+    Returns (grad_value, grad_sampling_locations, grad_attention_logits)."""
+    return msda_backward(grad_output, value, spatial_shapes, level_start_index, sampling_locations,
+                         attention_logits, value_layout, sampling_locations_layout, align_corners, padding_mode,
+                         compute_grad_value, compute_grad_sampling_locations, compute_grad_attention_logits,
+                         grad_value=grad_value, grad_sampling_locations=grad_sampling_locations,
+                         grad_attention_weights=grad_attention_logits, workspace=workspace, _logits=True)

@@ -414,7 +414,8 @@ int backward_entry(const msda_desc *desc, const void *grad_output, const void *v
                    const void *sampling_locations, const void *attention_weights, int compute_grad_value,
                    int compute_grad_sampling_locations, int compute_grad_attention_weights, void *grad_value,
                    void *grad_sampling_locations, void *grad_attention_weights, void *workspace,
-                   size_t workspace_bytes, bool allow_sort, cudaStream_t stream) {
+                   size_t workspace_bytes, BwdMode mode, cudaStream_t stream) {
+    const bool allow_sort = mode.allow_sort, accumulate = mode.accumulate;
     int rc = validate_desc(desc);
     if (rc) return rc;
     const msda_desc *d = desc;
@@ -425,7 +426,7 @@ int backward_entry(const msda_desc *desc, const void *grad_output, const void *v
     const int64_t value_elems = d->B * d->L * d->N_h * d->C_h;
     const int64_t go_elems = d->B * d->N_q * d->N_h * d->C_h;
     const bool need_v = (fl || fa) && samples > 0 && d->C_h > 0;
-    const bool need_a = (fv || fl) && samples > 0;
+    const bool need_a = (fv || fl || (mode.logits && fa)) && samples > 0;
     if (samples > 0 && !sampling_locations) return MSDA_ERR_NULL_POINTER;
     if (samples > 0 && go_elems > 0 && !grad_output) return MSDA_ERR_NULL_POINTER;
     if (need_v && !value) return MSDA_ERR_NULL_POINTER;
@@ -434,7 +435,7 @@ int backward_entry(const msda_desc *desc, const void *grad_output, const void *v
     if (fl && samples > 0 && !grad_sampling_locations) return MSDA_ERR_NULL_POINTER;
     if (fa && samples > 0 && !grad_attention_weights) return MSDA_ERR_NULL_POINTER;
     const size_t es = value_elem_size(d);
-    if (!aligned(grad_output, es) || !aligned(value, es) || !aligned(grad_value, es) ||
+    if (!aligned(grad_output, es) || !aligned(value, es) || !aligned(grad_value, accumulate ? 4 : es) ||
         !aligned(sampling_locations, 4) || !aligned(attention_weights, 4) ||
         !aligned(grad_sampling_locations, 4) || !aligned(grad_attention_weights, 4))
         return MSDA_ERR_MISALIGNED;
@@ -448,7 +449,9 @@ int backward_entry(const msda_desc *desc, const void *grad_output, const void *v
     unsigned char *ws = (unsigned char *)workspace;
     BwdBuffers bb;
     memset(&bb, 0, sizeof(bb));
-    bb.gv_acc = fv ? (bf16 ? (float *)(ws + plan.acc_off) : (float *)grad_value) : nullptr;
+    // the binary32 accumulator: the caller's (accumulate), grad_value itself
+    // (binary32 value) or the workspace (bfloat16 value)
+    bb.gv_acc = fv ? ((bf16 && !accumulate) ? (float *)(ws + plan.acc_off) : (float *)grad_value) : nullptr;
     bb.grad_loc = (float *)grad_sampling_locations;
     bb.grad_attn = (float *)grad_attention_weights;
     if (plan.sort) {
@@ -465,10 +468,11 @@ int backward_entry(const msda_desc *desc, const void *grad_output, const void *v
     if (rc) return rc;
     Params p = make_params(d, cfg, V);
     p.flags = (fv ? kGradValue : 0) | (fl ? kGradLoc : 0) | (fa ? kGradAttn : 0);
+    p.logits = mode.logits ? 1 : 0;
     p.n_sm = samples > 0 ? sm_count() : 0;
 
     cudaError_t e = cudaSuccess;
-    if (fv) e = launch_zero_f32(bb.gv_acc, value_elems, stream);
+    if (fv && !accumulate) e = launch_zero_f32(bb.gv_acc, value_elems, stream);
     const bool sort = plan.sort && !fl && !fa;
     if (e == cudaSuccess && samples > 0 && sort) e = launch_sort_keys(p, (const float *)sampling_locations, bb, stream);
     if (e == cudaSuccess && samples > 0) {
@@ -492,16 +496,12 @@ int backward_entry(const msda_desc *desc, const void *grad_output, const void *v
             e = cfg.vec ? launch_gv_reduce<float, true>(p, cfg.G, cfg.NCH, (const float *)grad_output, bb, stream)
                         : launch_gv_reduce<float, false>(p, cfg.G, cfg.NCH, (const float *)grad_output, bb, stream);
     }
-    if (e == cudaSuccess && fv && bf16) e = launch_f32_to_bf16(bb.gv_acc, (__nv_bfloat16 *)grad_value, value_elems, stream);
+    if (e == cudaSuccess && fv && bf16 && !accumulate) e = launch_f32_to_bf16(bb.gv_acc, (__nv_bfloat16 *)grad_value, value_elems, stream);
     return record_cuda(e);
 }
 
-}  // namespace msda
-
-extern "C" {
-
-int msda_forward(const msda_desc *desc, const void *value, const void *sampling_locations,
-                 const void *attention_weights, void *out, cudaStream_t stream) {
+int forward_entry(const msda_desc *desc, const void *value, const void *sampling_locations,
+                  const void *attention_weights, void *out, bool logits, cudaStream_t stream) {
     int rc = validate_desc(desc);
     if (rc) return rc;
     const msda_desc *d = desc;
@@ -524,6 +524,7 @@ int msda_forward(const msda_desc *desc, const void *value, const void *sampling_
     if (out_elems == 0) return MSDA_OK;
     Params p = make_params(d, cfg, V);
     p.n_sm = sm_count();
+    p.logits = logits ? 1 : 0;
     cudaError_t e;
     if (d->value_dtype == MSDA_DTYPE_F32)
         e = msda::launch_forward<float>(p, cfg.vec, cfg.G, cfg.NCH, (const float *)value,
@@ -534,6 +535,15 @@ int msda_forward(const msda_desc *desc, const void *value, const void *sampling_
                                                 (const float *)sampling_locations,
                                                 (const float *)attention_weights, (__nv_bfloat16 *)out, stream);
     return record_cuda(e);
+}
+
+}  // namespace msda
+
+extern "C" {
+
+int msda_forward(const msda_desc *desc, const void *value, const void *sampling_locations,
+                 const void *attention_weights, void *out, cudaStream_t stream) {
+    return msda::forward_entry(desc, value, sampling_locations, attention_weights, out, false, stream);
 }
 
 size_t msda_backward_workspace_size(const msda_desc *desc, int compute_grad_value) {
@@ -547,8 +557,35 @@ int msda_backward(const msda_desc *desc, const void *grad_output, const void *va
                   size_t workspace_bytes, cudaStream_t stream) {
     return msda::backward_entry(desc, grad_output, value, sampling_locations, attention_weights, compute_grad_value,
                                 compute_grad_sampling_locations, compute_grad_attention_weights, grad_value,
-                                grad_sampling_locations, grad_attention_weights, workspace, workspace_bytes, true,
-                                stream);
+                                grad_sampling_locations, grad_attention_weights, workspace, workspace_bytes,
+                                msda::BwdMode{true, false, false}, stream);
+}
+
+int msda_backward_accumulate(const msda_desc *desc, const void *grad_output, const void *value,
+                             const void *sampling_locations, const void *attention_weights, int compute_grad_value,
+                             int compute_grad_sampling_locations, int compute_grad_attention_weights,
+                             float *grad_value_accum, void *grad_sampling_locations, void *grad_attention_weights,
+                             void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+    return msda::backward_entry(desc, grad_output, value, sampling_locations, attention_weights, compute_grad_value,
+                                compute_grad_sampling_locations, compute_grad_attention_weights, grad_value_accum,
+                                grad_sampling_locations, grad_attention_weights, workspace, workspace_bytes,
+                                msda::BwdMode{true, true, false}, stream);
+}
+
+int msda_forward_logits(const msda_desc *desc, const void *value, const void *sampling_locations,
+                        const void *attention_logits, void *out, cudaStream_t stream) {
+    return msda::forward_entry(desc, value, sampling_locations, attention_logits, out, true, stream);
+}
+
+int msda_backward_logits(const msda_desc *desc, const void *grad_output, const void *value,
+                         const void *sampling_locations, const void *attention_logits, int compute_grad_value,
+                         int compute_grad_sampling_locations, int compute_grad_attention_logits,
+                         void *grad_value, void *grad_sampling_locations, void *grad_attention_logits,
+                         void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+    return msda::backward_entry(desc, grad_output, value, sampling_locations, attention_logits, compute_grad_value,
+                                compute_grad_sampling_locations, compute_grad_attention_logits, grad_value,
+                                grad_sampling_locations, grad_attention_logits, workspace, workspace_bytes,
+                                msda::BwdMode{true, false, true}, stream);
 }
 
 const char *msda_status_string(int status) {

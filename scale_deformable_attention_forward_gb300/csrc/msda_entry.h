@@ -10,11 +10,27 @@ namespace msda {
 // only); true lets the library choose the cell-sorted grad_value.
 size_t backward_workspace_bytes(const msda_desc *desc, int compute_grad_value, bool allow_sort);
 
-// msda_backward's argument checks and work, with the same allow_sort choice.
+// How a backward entry point differs from msda_backward:
+//   allow_sort  as for backward_workspace_bytes;
+//   accumulate  grad_value is a caller-owned binary32 accumulator (value's
+//               shape and layout) that this call's grad_value is added to,
+//               without zeroing and without conversion;
+//   logits      attention_weights holds logits (softmax over each row's
+//               N_l*N_p slots gives the weights) and grad_attention_weights
+//               receives the logits' gradient.
+struct BwdMode {
+    bool allow_sort, accumulate, logits;
+};
+
+// msda_backward's argument checks and work, in the given mode.
 int backward_entry(const msda_desc *desc, const void *grad_output, const void *value,
                    const void *sampling_locations, const void *attention_weights, int compute_grad_value,
                    int compute_grad_sampling_locations, int compute_grad_attention_weights, void *grad_value,
                    void *grad_sampling_locations, void *grad_attention_weights, void *workspace,
-                   size_t workspace_bytes, bool allow_sort, cudaStream_t stream);
+                   size_t workspace_bytes, BwdMode mode, cudaStream_t stream);
+
+// msda_forward's argument checks and work; logits as in BwdMode.
+int forward_entry(const msda_desc *desc, const void *value, const void *sampling_locations,
+                  const void *attention_weights, void *out, bool logits, cudaStream_t stream);
 
 }  // namespace msda

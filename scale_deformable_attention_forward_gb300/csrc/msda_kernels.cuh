@@ -54,6 +54,7 @@ struct Params {
     FastDiv div_q, div_h, div_p, div_nlp;  // by N_q, N_h, N_p, N_l * N_p
     int padding;    // 0 zeros, 1 border (used when the kernel is not specialised)
     int flags;      // kGradValue | kGradLoc | kGradAttn (backward)
+    int logits;     // 1: `attention_weights` holds logits; A = softmax over the row's N_l*N_p of them
     // value (and grad_value / accumulator) element strides
     int64_t v_sB;
     int v_sH, v_sP;
@@ -320,13 +321,37 @@ __device__ __forceinline__ RowRange block_rows(const Params &p) {
     return rr;
 }
 
+// Softmax of one row's N_l*N_p attention logits (the attention weights the
+// workloads are built from), over the G lanes of its group: every lane ends
+// with the row maximum m and 1 / sum_j exp(x_j - m), and the weight of sample
+// j is then exp(x_j - m) times the latter.
+template <int G>
+__device__ __forceinline__ float2 row_softmax_stats(const float *ap, int NLP, int r, unsigned gmask) {
+    float m = -INFINITY;
+    for (int j = r; j < NLP; j += G) m = fmaxf(m, __ldg(ap + j));
+#pragma unroll
+    for (int o = G / 2; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(gmask, m, o));
+    float sum = 0.0f;
+    for (int j = r; j < NLP; j += G) sum += expf(__ldg(ap + j) - m);
+#pragma unroll
+    for (int o = G / 2; o >= 1; o >>= 1) sum += __shfl_xor_sync(gmask, sum, o);
+    return make_float2(m, 1.0f / sum);
+}
+
 // ---------------------------------------------------------------- forward
 #ifndef MSDA_FWD_MIN_BLOCKS
-#define MSDA_FWD_MIN_BLOCKS 3
+#define MSDA_FWD_MIN_BLOCKS 4
 #endif
-// Blocks per SM the row kernels are compiled for (registers a thread: 85 for
-// rows of up to 8 elements a lane, 128 for the wide-row kernels).
-__host__ __device__ constexpr int row_min_blocks(int elems) { return elems <= 8 ? MSDA_FWD_MIN_BLOCKS : 2; }
+#ifndef MSDA_BWD_MIN_BLOCKS
+#define MSDA_BWD_MIN_BLOCKS 3
+#endif
+// Blocks per SM the row kernels are compiled for, for rows of up to 8
+// elements a lane: the forward 4 (64 registers a thread: more warps to hide
+// the gather latency), the backward 3 (85 registers: its per-sample partials
+// and reduction need them); 2 (128 registers) for the wide-row kernels.
+__host__ __device__ constexpr int row_min_blocks(int elems, bool fwd) {
+    return elems <= 8 ? (fwd ? MSDA_FWD_MIN_BLOCKS : MSDA_BWD_MIN_BLOCKS) : 2;
+}
 
 // One sample's cell in the form the lanes of a group exchange (six 32-bit
 // shuffles): o0 is the element offset (relative to the (b, h) slice of value)
@@ -365,7 +390,7 @@ __device__ __forceinline__ FwdCell fwd_cell(const Cell &c, float A, int W, int H
 // (lane r owns chunks r, r+G, ...), two samples' corners in flight.
 // PAD: 0 zeros, 1 border, -1 read p.padding at run time.
 template <typename T, int VEC, int G, int NCH, int PAD>
-__global__ void __launch_bounds__(kThreads, row_min_blocks(NCH *VEC))
+__global__ void __launch_bounds__(kThreads, row_min_blocks(NCH *VEC, true))
 msda_forward_kernel(const __grid_constant__ Params p, const T *__restrict__ value, const float *__restrict__ loc,
                     const float *__restrict__ attn, T *__restrict__ out) {
     __shared__ LevelTables lt;
@@ -386,6 +411,7 @@ msda_forward_kernel(const __grid_constant__ Params p, const T *__restrict__ valu
         const T *vbh = value + rw.b * p.v_sB + (int64_t)rw.h * p.v_sH + r * VEC;
         const float *lp = loc + rw.b * p.l_sB + (int64_t)((rw.q * (uint32_t)p.N_h + rw.h) * (uint32_t)NLP) * sJ;
         const float *ap = attn + (int64_t)rw.bqh * NLP;
+        const float2 sm = p.logits ? row_softmax_stats<G>(ap, NLP, r, gmask) : make_float2(0.0f, 1.0f);
 
         float acc[NCH][VEC];
 #pragma unroll
@@ -398,7 +424,9 @@ msda_forward_kernel(const __grid_constant__ Params p, const T *__restrict__ valu
             FwdCell mine = {0, 0, 0.0f, 0.0f, 0.0f, 0.0f};
             const int j = j0 + r;
             if (j < NLP) {
-                const float u = __ldg(lp + j * sJ), v = __ldg(lp + j * sJ + sXY), A = __ldg(ap + j);
+                const float u = __ldg(lp + j * sJ), v = __ldg(lp + j * sJ + sXY);
+                float A = __ldg(ap + j);
+                if (p.logits) A = expf(A - sm.x) * sm.y;
                 const int l = (int)p.div_p.div((uint32_t)j);
                 const int W = lt.W[l], H = lt.H[l];
                 const Cell c = make_cell<PAD>(u, v, lt.sx[l], lt.sy[l], p.off, W, H, p.padding);
@@ -507,7 +535,7 @@ __device__ __forceinline__ int cell_key(const Cell &c, int W, int kst) {
 // kGradLoc|kGradAttn (no grad_value; the two others as p.flags says), or -1
 // (everything from p.flags at run time).  PAD as in the forward.
 template <typename T, int VEC, int G, int NCH, int PAD, int FL, bool SORT>
-__global__ void __launch_bounds__(kThreads, row_min_blocks(NCH *VEC))
+__global__ void __launch_bounds__(kThreads, row_min_blocks(NCH *VEC, false))
 msda_backward_kernel(const __grid_constant__ Params p, const T *__restrict__ grad_out, const T *__restrict__ value,
                      const float *__restrict__ loc, const float *__restrict__ attn, float *__restrict__ gv_acc,
                      float *__restrict__ grad_loc, float *__restrict__ grad_attn, int *__restrict__ cursor,
@@ -520,7 +548,8 @@ msda_backward_kernel(const __grid_constant__ Params p, const T *__restrict__ gra
     const int flags = FL < 0 ? p.flags : (FL == (kGradLoc | kGradAttn) ? (p.flags & FL) : FL);
     const bool want_gv = flags & kGradValue, want_gl = flags & kGradLoc, want_ga = flags & kGradAttn;
     const bool need_v = want_gl || want_ga;  // value is read only for these two
-    const bool need_a = want_gv || want_gl;  // attention is read only for these two
+    // attention is read only for these two, and for the logits' gradient
+    const bool need_a = want_gv || want_gl || (p.logits && want_ga);
     const bool scatter = want_gv && !SORT;   // consumers add into grad_value
     const int lane = threadIdx.x & 31;
     const int r = lane & (G - 1);
@@ -545,6 +574,9 @@ msda_backward_kernel(const __grid_constant__ Params p, const T *__restrict__ gra
         float *glp = grad_loc + lrow;
         const float *ap = attn + (int64_t)rw.bqh * NLP;
         float *gap = grad_attn + (int64_t)rw.bqh * NLP;
+        const bool soft = p.logits && need_a;
+        const float2 sm = soft ? row_softmax_stats<G>(ap, NLP, r, gmask) : make_float2(0.0f, 1.0f);
+        float sAg = 0.0f;  // (logits) this lane's part of sum_j A_j <g, S_j>
         float g[NCH][VEC];
         {
             const T *src = grad_out + (int64_t)rw.bqh * p.C_h + r * VEC;
@@ -574,6 +606,7 @@ msda_backward_kernel(const __grid_constant__ Params p, const T *__restrict__ gra
                     u = __ldg(lp + j * sJ);
                     v = __ldg(lp + j * sJ + sXY);
                     if (need_a) A = __ldg(ap + j);
+                    if (soft) A = expf(A - sm.x) * sm.y;
                 }
                 const int W = lt.W[l], H = lt.H[l];
                 c = make_cell<PAD>(u, v, lt.sx[l], lt.sy[l], p.off, W, H, p.padding);
@@ -666,12 +699,23 @@ msda_backward_kernel(const __grid_constant__ Params p, const T *__restrict__ gra
                         tx = fmaf(dwx[i], di, tx);
                         ty = fmaf(dwy[i], di, ty);
                     }
-                    if (want_ga) gap[j] = ga;
+                    if (want_ga) gap[j] = ga;  // (logits: <g, S_j>, turned into d/dlogit below)
+                    if (soft) sAg = fmaf(A, ga, sAg);
                     if (want_gl) {
                         glp[j * sJ] = A * tx * (lt.sx[l] * c.kx);
                         glp[j * sJ + sXY] = A * ty * (lt.sy[l] * c.ky);
                     }
                 }
+            }
+        }
+        if (soft && want_ga) {
+            // d/dlogit_j = A_j (<g, S_j> - sum_k A_k <g, S_k>); lane r rewrites the
+            // samples it stored above
+#pragma unroll
+            for (int o = G / 2; o >= 1; o >>= 1) sAg += __shfl_xor_sync(gmask, sAg, o);
+            for (int j = r; j < NLP; j += G) {
+                const float A = expf(__ldg(ap + j) - sm.x) * sm.y;
+                gap[j] = A * (gap[j] - sAg);
             }
         }
     }

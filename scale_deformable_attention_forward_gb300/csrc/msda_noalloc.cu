@@ -98,5 +98,5 @@ extern "C" int msda_backward_noalloc(const msda_desc *desc, const void *grad_out
     return msda::backward_entry(desc, grad_output, value, sampling_locations, attention_weights,
                                 compute_grad_value, compute_grad_sampling_locations,
                                 compute_grad_attention_weights, grad_value, grad_sampling_locations,
-                                grad_attention_weights, ws, need, false, stream);
+                                grad_attention_weights, ws, need, msda::BwdMode{false, false, false}, stream);
 }

@@ -226,6 +226,7 @@ def generate(w: Workload, seed: Optional[int] = None) -> dict:
         raise ValueError(f"unknown location recipe {w.loc_recipe!r}")
 
     logits = rng.standard_normal((B, Nq, Nh, Nl * Np))
+    raw_logits = logits.reshape(B, Nq, Nh, Nl, Np).copy()
     if logits.size:
         logits -= logits.max(axis=-1, keepdims=True)
         e = np.exp(logits)
@@ -239,6 +240,7 @@ def generate(w: Workload, seed: Optional[int] = None) -> dict:
         "value": to_value_layout(store_dtype(value, w.dtype), w.value_layout),
         "sampling_locations": to_loc_layout(store_dtype(loc, "f32"), w.loc_layout),
         "attention_weights": store_dtype(attn, "f32"),
+        "attention_logits": store_dtype(raw_logits, "f32"),  # the logits the weights come from
         "grad_output": store_dtype(grad_output, w.dtype),
         "spatial_shapes": tuple(tuple(int(x) for x in hw) for hw in w.levels),
         "level_start_index": w.level_start_index,

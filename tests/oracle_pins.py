@@ -553,9 +553,55 @@ def pin_cell_decision_in_binary32(orc):
     assert out_f32[0, 0, 0] == float(k * k)
 
 
+def pin_attention_logits(orc):
+    """Attention logits (the fused softmax producer): the weights are a
+    softmax over each (b, q, h)'s N_l*N_p slots.  Pinned by: equal logits give
+    equal weights 1/(N_l*N_p); adding a constant to a row's logits changes
+    nothing; one dominant logit selects that sample; the logits' gradient sums
+    to zero over every row and matches central differences of <g, out>."""
+    rng = np.random.default_rng(131)
+    levels = ((5, 7), (3, 4))
+    B, N_q, N_h, C_h, N_p = 2, 3, 2, 3, 2
+    P = _problem(rng, levels, B, N_q, N_h, C_h, N_p)
+    nlp = len(levels) * N_p
+    z = rng.standard_normal(P["attn"].shape)
+    kw = dict(padding_mode="zeros", align_corners=False)
+
+    def fwd_z(zz):
+        return orc.forward_logits(P["value"], P["levels"], P["starts"], P["loc"], zz, **kw)
+
+    # equal logits
+    _close(fwd_z(np.full_like(z, 0.3)), _fwd(orc, P, attn=np.full_like(z, 1.0 / nlp), **kw), 1e-14, "equal logits")
+    # row shift
+    shift = rng.standard_normal(z.shape[:3])[..., None, None] * 5.0
+    _close(fwd_z(z + shift), fwd_z(z), 1e-13, "row shift")
+    # one dominant logit: sample (l=1, p=0) of every row
+    zd = np.zeros_like(z)
+    zd[..., 1, 0] = 60.0
+    onehot = np.zeros_like(z)
+    onehot[..., 1, 0] = 1.0
+    _close(fwd_z(zd), _fwd(orc, P, attn=onehot, **kw), 1e-13, "dominant logit")
+    # gradient: rows sum to zero; central differences of J = <g, out>
+    gv, gl, gz = orc.backward_logits(P["g"], P["value"], P["levels"], P["starts"], P["loc"], z, **kw)
+    assert np.max(np.abs(gz.reshape(B, N_q, N_h, -1).sum(-1))) < 1e-12, "logit gradient rows must sum to 0"
+    h = 1e-5
+    for idx in np.ndindex(*z.shape):
+        zp, zm = z.copy(), z.copy()
+        zp[idx] += h
+        zm[idx] -= h
+        fd = (np.sum(P["g"] * fwd_z(zp)) - np.sum(P["g"] * fwd_z(zm))) / (2 * h)
+        assert abs(fd - gz[idx]) <= 1e-8 * max(1.0, abs(gz[idx])), f"FD logits {idx}: {fd} vs {gz[idx]}"
+    # grad_value / grad_loc are those of the softmaxed weights
+    A = np.exp(z - z.max(axis=(-2, -1), keepdims=True))
+    A /= A.sum(axis=(-2, -1), keepdims=True)
+    gv2, gl2, _ = _bwd(orc, P, attn=A, **kw)
+    _close(gv, gv2, 1e-13, "grad_value with logits")
+    _close(gl, gl2, 1e-13, "grad_loc with logits")
+
+
 ALL_PINS = [
     pin_pixel_centre, pin_corner_points, pin_affine_bilinear_closed_form, pin_constant_map,
     pin_zeros_padding, pin_border_padding, pin_grid_sample, pin_linearity, pin_layouts,
     pin_grad_attention_is_sample_dot, pin_adjoint, pin_finite_differences, pin_compute_flags,
-    pin_hand_worked_example, pin_cell_decision_in_binary32,
+    pin_hand_worked_example, pin_cell_decision_in_binary32, pin_attention_logits,
 ]

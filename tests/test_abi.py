@@ -119,6 +119,21 @@ def test_rejections_backward(lib):
     assert _bwd(lib, bf, ws=ctypes.c_void_p(0x10004), ws_bytes=need) == -9
 
 
+@no_gpu
+def test_rejections_backward_accumulate(lib):
+    d = msda.make_desc(DIMS, LEVELS, STARTS)
+    P = ctypes.c_void_p
+
+    def acc_call(acc, flags=(1, 1, 1)):
+        lib.msda_backward_accumulate.argtypes = [ctypes.POINTER(msda.msda_desc), P, P, P, P, ctypes.c_int,
+                                                 ctypes.c_int, ctypes.c_int, P, P, P, P, ctypes.c_size_t, P]
+        return lib.msda_backward_accumulate(d.ref(), FAKE, FAKE, FAKE, FAKE, *flags, acc, FAKE, FAKE, None, 0, None)
+
+    assert acc_call(None) == -1                       # grad_value requested, no accumulator
+    assert acc_call(ctypes.c_void_p(0x10002)) == -9   # binary32 accumulator must be 4-byte aligned
+    assert acc_call(FAKE, flags=(0, 0, 0)) == -4
+
+
 def test_python_binding_rejects_cpu_tensors(lib):
     torch = pytest.importorskip("torch")
     v = torch.zeros(1, 30, 1, 4)
