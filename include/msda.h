@@ -74,8 +74,10 @@ enum msda_padding {
 
 /* Element types. */
 enum msda_dtype {
-    MSDA_DTYPE_F32 = 0, /* IEEE binary32 */
-    MSDA_DTYPE_BF16 = 1 /* bfloat16; arithmetic is binary32, stores round to nearest even */
+    MSDA_DTYPE_F32 = 0,  /* IEEE binary32 */
+    MSDA_DTYPE_BF16 = 1, /* bfloat16; arithmetic is binary32, stores round to nearest even */
+    MSDA_DTYPE_F16 = 2   /* IEEE binary16 (loc_dtype only); arithmetic is binary32, stores round
+                            to nearest even */
 };
 
 /* Status codes: 0 on success, negative on failure. */
@@ -89,7 +91,7 @@ enum msda_status {
                                    start[l+1] != start[l] + H_l*W_l, or L != sum H_l*W_l */
     MSDA_ERR_WORKSPACE = -6,    /* workspace smaller than msda_backward_workspace_size() */
     MSDA_ERR_TOO_LARGE = -7,    /* a size exceeds the 32-bit index limits stated below */
-    MSDA_ERR_UNSUPPORTED = -8,  /* a valid but unimplemented combination (loc_dtype BF16,
+    MSDA_ERR_UNSUPPORTED = -8,  /* a valid but unimplemented combination (value_dtype F16,
                                    C_h > 256 with unaligned pointers) */
     MSDA_ERR_MISALIGNED = -9,   /* a pointer not aligned to its element size */
     MSDA_ERR_CUDA = -10         /* the CUDA runtime reported an error (msda_last_cuda_error) */
@@ -114,8 +116,10 @@ typedef struct msda_desc {
     int32_t padding_mode;             /* enum msda_padding */
     int32_t value_dtype;              /* enum msda_dtype of value, out, grad_output, grad_value */
     int32_t loc_dtype;                /* enum msda_dtype of sampling_locations,
-                                         attention_weights and their gradients
-                                         (only MSDA_DTYPE_F32 is implemented) */
+                                         attention_weights (or logits) and their
+                                         gradients: F32, BF16 or F16.  The pages
+                                         leave it open; 16-bit locations quantise
+                                         a 167-pixel level to ~0.3-1 pixel */
 } msda_desc;
 
 /* Forward ("MS Deformable Attention Kernel API Reference", Parameters and

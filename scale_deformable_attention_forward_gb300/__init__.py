@@ -29,7 +29,7 @@ _LIB_PATH = os.path.join(_PKG, "_build", "libmsda.so")
 VALUE_LAYOUTS = {"BLNC": 0, "BNLC": 1}
 LOC_LAYOUTS = {"BQHLP2": 0, "B2QHLP": 1}
 PADDING_MODES = {"zeros": 0, "border": 1}
-DTYPE_F32, DTYPE_BF16 = 0, 1
+DTYPE_F32, DTYPE_BF16, DTYPE_F16 = 0, 1, 2
 MAX_LEVELS = 16
 
 
@@ -181,6 +181,15 @@ def _value_dtype(t):
     raise TypeError(f"value must be float32 or bfloat16, got {t.dtype}")
 
 
+def _loc_dtype(t):
+    """msda_dtype of sampling_locations / attention weights (and their gradients)."""
+    torch = _torch()
+    codes = {torch.float32: DTYPE_F32, torch.bfloat16: DTYPE_BF16, torch.float16: DTYPE_F16}
+    if t.dtype not in codes:
+        raise TypeError(f"sampling_locations must be float32, bfloat16 or float16, got {t.dtype}")
+    return codes[t.dtype]
+
+
 def _check(t, name, dtype, shape, device):
     torch = _torch()
     if not isinstance(t, torch.Tensor):
@@ -226,14 +235,15 @@ def msda_forward(value, spatial_shapes, level_start_index, sampling_locations, a
                          f"sampling_locations has {N_l}")
     vdt = _value_dtype(value)
     _check(value, "value", value.dtype, value.shape, dev)
-    _check(sampling_locations, "sampling_locations", torch.float32, sampling_locations.shape, dev)
-    _check(attention_weights, "attention_weights", torch.float32, (B, N_q, N_h, N_l, N_p), dev)
+    ldt = _loc_dtype(sampling_locations)
+    _check(sampling_locations, "sampling_locations", sampling_locations.dtype, sampling_locations.shape, dev)
+    _check(attention_weights, "attention_weights", sampling_locations.dtype, (B, N_q, N_h, N_l, N_p), dev)
     if out is None:
         out = torch.empty((B, N_q, N_h * C_h), dtype=value.dtype, device=dev)
     else:
         _check(out, "out", value.dtype, (B, N_q, N_h * C_h), dev)
     d = make_desc((B, N_q, N_h, C_h, N_l, N_p, L), shapes, starts, value_layout,
-                  sampling_locations_layout, align_corners, padding_mode, vdt)
+                  sampling_locations_layout, align_corners, padding_mode, vdt, ldt)
     fn, name = (lib.msda_forward_logits, "msda_forward_logits") if _logits else (lib.msda_forward, "msda_forward")
     with torch.cuda.device(dev):
         rc = fn(d.ref(), _ptr(value), _ptr(sampling_locations), _ptr(attention_weights), _ptr(out), _stream(dev))
@@ -291,8 +301,9 @@ def msda_backward(grad_output, value, spatial_shapes, level_start_index, samplin
     vdt = _value_dtype(value)
     _check(value, "value", value.dtype, value.shape, dev)
     _check(grad_output, "grad_output", value.dtype, (B, N_q, N_h * C_h), dev)
-    _check(sampling_locations, "sampling_locations", torch.float32, sampling_locations.shape, dev)
-    _check(attention_weights, "attention_weights", torch.float32, (B, N_q, N_h, N_l, N_p), dev)
+    ldt = _loc_dtype(sampling_locations)
+    _check(sampling_locations, "sampling_locations", sampling_locations.dtype, sampling_locations.shape, dev)
+    _check(attention_weights, "attention_weights", sampling_locations.dtype, (B, N_q, N_h, N_l, N_p), dev)
     fv, fl, fa = (bool(compute_grad_value), bool(compute_grad_sampling_locations),
                   bool(compute_grad_attention_weights))
     if not (fv or fl or fa):
@@ -312,17 +323,19 @@ def msda_backward(grad_output, value, spatial_shapes, level_start_index, samplin
     if fl:
         if grad_sampling_locations is None:
             grad_sampling_locations = torch.empty_like(sampling_locations)
-        _check(grad_sampling_locations, "grad_sampling_locations", torch.float32, sampling_locations.shape, dev)
+        _check(grad_sampling_locations, "grad_sampling_locations", sampling_locations.dtype,
+               sampling_locations.shape, dev)
     else:
         grad_sampling_locations = None
     if fa:
         if grad_attention_weights is None:
             grad_attention_weights = torch.empty_like(attention_weights)
-        _check(grad_attention_weights, "grad_attention_weights", torch.float32, attention_weights.shape, dev)
+        _check(grad_attention_weights, "grad_attention_weights", sampling_locations.dtype,
+               attention_weights.shape, dev)
     else:
         grad_attention_weights = None
     d = make_desc((B, N_q, N_h, C_h, N_l, N_p, L), shapes, starts, value_layout,
-                  sampling_locations_layout, align_corners, padding_mode, vdt)
+                  sampling_locations_layout, align_corners, padding_mode, vdt, ldt)
     ws_bytes = int(lib.msda_backward_workspace_size(d.ref(), int(fv)))
     if ws_bytes > 0:
         if workspace is None:

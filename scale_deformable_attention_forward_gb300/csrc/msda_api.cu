@@ -26,6 +26,7 @@ int record_cuda(cudaError_t e) {
 bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
 
 size_t value_elem_size(const msda_desc *d) { return d->value_dtype == MSDA_DTYPE_BF16 ? 2 : 4; }
+size_t loc_elem_size(const msda_desc *d) { return d->loc_dtype == MSDA_DTYPE_F32 ? 4 : 2; }
 
 // Shape, enum and level checks shared by every entry point ("MS Deformable
 // Attention Kernel API Reference", Parameters: spatial_shapes,
@@ -36,8 +37,10 @@ int validate_desc(const msda_desc *d) {
     if (d->loc_layout != MSDA_LAYOUT_BQHLP2 && d->loc_layout != MSDA_LAYOUT_B2QHLP) return MSDA_ERR_BAD_ENUM;
     if (d->padding_mode != MSDA_PADDING_ZEROS && d->padding_mode != MSDA_PADDING_BORDER) return MSDA_ERR_BAD_ENUM;
     if (d->align_corners != 0 && d->align_corners != 1) return MSDA_ERR_BAD_ENUM;
-    if (d->value_dtype != MSDA_DTYPE_F32 && d->value_dtype != MSDA_DTYPE_BF16) return MSDA_ERR_BAD_ENUM;
-    if (d->loc_dtype != MSDA_DTYPE_F32 && d->loc_dtype != MSDA_DTYPE_BF16) return MSDA_ERR_BAD_ENUM;
+    if (d->value_dtype != MSDA_DTYPE_F32 && d->value_dtype != MSDA_DTYPE_BF16 && d->value_dtype != MSDA_DTYPE_F16)
+        return MSDA_ERR_BAD_ENUM;
+    if (d->loc_dtype != MSDA_DTYPE_F32 && d->loc_dtype != MSDA_DTYPE_BF16 && d->loc_dtype != MSDA_DTYPE_F16)
+        return MSDA_ERR_BAD_ENUM;
     if (d->B < 0 || d->N_q < 0 || d->N_h < 0 || d->C_h < 0 || d->N_l < 0 || d->N_p < 0 || d->L < 0)
         return MSDA_ERR_BAD_DIM;
     if (d->N_l > MSDA_MAX_LEVELS) return MSDA_ERR_BAD_DIM;
@@ -61,7 +64,7 @@ int validate_desc(const msda_desc *d) {
     if (d->N_h > 0 && d->C_h > 0 && d->L + 2 * wmax + 4 > kIndexLimit / d->N_h / d->C_h) return MSDA_ERR_TOO_LARGE;
     if (d->N_q > 0 && d->N_h > 0 && nlp > 0 && d->N_q > kIndexLimit / 2 / d->N_h / nlp) return MSDA_ERR_TOO_LARGE;
     if (d->B > 0 && d->N_q > 0 && d->N_h > 0 && d->B > kIndexLimit / d->N_q / d->N_h) return MSDA_ERR_TOO_LARGE;
-    if (d->loc_dtype != MSDA_DTYPE_F32) return MSDA_ERR_UNSUPPORTED;
+    if (d->value_dtype == MSDA_DTYPE_F16) return MSDA_ERR_UNSUPPORTED;  // value: binary32 or bfloat16 only
     return MSDA_OK;
 }
 
@@ -111,6 +114,7 @@ Params make_params(const msda_desc *d, const Config &cfg, int V_vec) {
     p.div_p = make_fastdiv((uint32_t)d->N_p);
     p.div_nlp = make_fastdiv((uint32_t)(d->N_l * d->N_p));
     p.padding = d->padding_mode;
+    p.loc_dt = d->loc_dtype == MSDA_DTYPE_F32 ? 0 : d->loc_dtype == MSDA_DTYPE_BF16 ? 1 : 2;
     p.flags = 0;
     if (d->value_layout == MSDA_LAYOUT_BLNC) {
         p.v_sB = d->L * d->N_h * d->C_h;
@@ -436,8 +440,8 @@ int backward_entry(const msda_desc *desc, const void *grad_output, const void *v
     if (fa && samples > 0 && !grad_attention_weights) return MSDA_ERR_NULL_POINTER;
     const size_t es = value_elem_size(d);
     if (!aligned(grad_output, es) || !aligned(value, es) || !aligned(grad_value, accumulate ? 4 : es) ||
-        !aligned(sampling_locations, 4) || !aligned(attention_weights, 4) ||
-        !aligned(grad_sampling_locations, 4) || !aligned(grad_attention_weights, 4))
+        !aligned(sampling_locations, loc_elem_size(d)) || !aligned(attention_weights, loc_elem_size(d)) ||
+        !aligned(grad_sampling_locations, loc_elem_size(d)) || !aligned(grad_attention_weights, loc_elem_size(d)))
         return MSDA_ERR_MISALIGNED;
     const bool bf16 = d->value_dtype == MSDA_DTYPE_BF16;
     const BwdPlan plan = plan_backward(d, fv, allow_sort);
@@ -513,8 +517,8 @@ int forward_entry(const msda_desc *desc, const void *value, const void *sampling
         (reads && value_elems > 0 && !value))
         return MSDA_ERR_NULL_POINTER;
     const size_t es = value_elem_size(d);
-    if (!aligned(value, es) || !aligned(out, es) || !aligned(sampling_locations, 4) ||
-        !aligned(attention_weights, 4))
+    if (!aligned(value, es) || !aligned(out, es) || !aligned(sampling_locations, loc_elem_size(d)) ||
+        !aligned(attention_weights, loc_elem_size(d)))
         return MSDA_ERR_MISALIGNED;
     Config cfg;
     const int V = d->value_dtype == MSDA_DTYPE_BF16 ? msda::VecWidth<__nv_bfloat16>::value
@@ -598,7 +602,7 @@ const char *msda_status_string(int status) {
     case MSDA_ERR_LEVELS: return "spatial_shapes / level_start_index / L are inconsistent";
     case MSDA_ERR_WORKSPACE: return "workspace is smaller than msda_backward_workspace_size()";
     case MSDA_ERR_TOO_LARGE: return "a size exceeds the library's 32-bit index limits";
-    case MSDA_ERR_UNSUPPORTED: return "valid but unsupported combination (bf16 locations, or C_h > 256 unaligned)";
+    case MSDA_ERR_UNSUPPORTED: return "valid but unsupported combination (binary16 value, or C_h > 256 unaligned)";
     case MSDA_ERR_MISALIGNED: return "a pointer is not aligned to its element size";
     case MSDA_ERR_CUDA: return "the CUDA runtime reported an error (see msda_last_cuda_error)";
     default: return "unknown status";

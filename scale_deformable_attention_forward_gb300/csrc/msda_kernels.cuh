@@ -26,6 +26,7 @@
 
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
 
 namespace msda {
@@ -55,6 +56,7 @@ struct Params {
     int padding;    // 0 zeros, 1 border (used when the kernel is not specialised)
     int flags;      // kGradValue | kGradLoc | kGradAttn (backward)
     int logits;     // 1: `attention_weights` holds logits; A = softmax over the row's N_l*N_p of them
+    int loc_dt;     // dtype of locations, weights and their gradients: 0 binary32, 1 bfloat16, 2 binary16
     // value (and grad_value / accumulator) element strides
     int64_t v_sB;
     int v_sH, v_sP;
@@ -166,6 +168,29 @@ template <> struct RedIO<8> {
         red_add_v4(p + 4, s * v[4], s * v[5], s * v[6], s * v[7]);
     }
 };
+
+// Locations, attention weights and their gradients in their storage dtype
+// (dt: 0 binary32, 1 bfloat16, 2 binary16), addressed by element index from
+// the tensor's base; arithmetic is binary32, stores round to nearest even.
+__device__ __forceinline__ float ldl(const float *base, int64_t i, int dt) {
+    if (dt == 0) return __ldg(base + i);
+    const unsigned short bits = __ldg(reinterpret_cast<const unsigned short *>(base) + i);
+    if (dt == 1) return __uint_as_float((uint32_t)bits << 16);  // bfloat16 -> binary32 is exact
+    return __half2float(__ushort_as_half(bits));
+}
+// The same for an element this thread wrote earlier in the kernel (not
+// through the read-only path).
+__device__ __forceinline__ float ldl_own(const float *base, int64_t i, int dt) {
+    if (dt == 0) return base[i];
+    const unsigned short bits = reinterpret_cast<const unsigned short *>(base)[i];
+    if (dt == 1) return __uint_as_float((uint32_t)bits << 16);
+    return __half2float(__ushort_as_half(bits));
+}
+__device__ __forceinline__ void stl(float *base, int64_t i, float v, int dt) {
+    if (dt == 0) base[i] = v;
+    else if (dt == 1) reinterpret_cast<__nv_bfloat16 *>(base)[i] = __float2bfloat16_rn(v);
+    else reinterpret_cast<__half *>(base)[i] = __float2half_rn(v);
+}
 
 // ---------------------------------------------------------------- geometry
 struct Row {
@@ -326,13 +351,14 @@ __device__ __forceinline__ RowRange block_rows(const Params &p) {
 // with the row maximum m and 1 / sum_j exp(x_j - m), and the weight of sample
 // j is then exp(x_j - m) times the latter.
 template <int G>
-__device__ __forceinline__ float2 row_softmax_stats(const float *ap, int NLP, int r, unsigned gmask) {
+__device__ __forceinline__ float2 row_softmax_stats(const float *attn, int64_t ao, int NLP, int r, unsigned gmask,
+                                                    int dt) {
     float m = -INFINITY;
-    for (int j = r; j < NLP; j += G) m = fmaxf(m, __ldg(ap + j));
+    for (int j = r; j < NLP; j += G) m = fmaxf(m, ldl(attn, ao + j, dt));
 #pragma unroll
     for (int o = G / 2; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(gmask, m, o));
     float sum = 0.0f;
-    for (int j = r; j < NLP; j += G) sum += expf(__ldg(ap + j) - m);
+    for (int j = r; j < NLP; j += G) sum += expf(ldl(attn, ao + j, dt) - m);
 #pragma unroll
     for (int o = G / 2; o >= 1; o >>= 1) sum += __shfl_xor_sync(gmask, sum, o);
     return make_float2(m, 1.0f / sum);
@@ -409,9 +435,10 @@ msda_forward_kernel(const __grid_constant__ Params p, const T *__restrict__ valu
     for (uint32_t row = rr.beg + threadIdx.x / G; row < rr.end; row += rr.step) {
         const Row rw = decode_row(p, row);
         const T *vbh = value + rw.b * p.v_sB + (int64_t)rw.h * p.v_sH + r * VEC;
-        const float *lp = loc + rw.b * p.l_sB + (int64_t)((rw.q * (uint32_t)p.N_h + rw.h) * (uint32_t)NLP) * sJ;
-        const float *ap = attn + (int64_t)rw.bqh * NLP;
-        const float2 sm = p.logits ? row_softmax_stats<G>(ap, NLP, r, gmask) : make_float2(0.0f, 1.0f);
+        const int64_t lo = rw.b * p.l_sB + (int64_t)((rw.q * (uint32_t)p.N_h + rw.h) * (uint32_t)NLP) * sJ;
+        const int64_t ao = (int64_t)rw.bqh * NLP;
+        const float2 sm =
+            p.logits ? row_softmax_stats<G>(attn, ao, NLP, r, gmask, p.loc_dt) : make_float2(0.0f, 1.0f);
 
         float acc[NCH][VEC];
 #pragma unroll
@@ -424,8 +451,8 @@ msda_forward_kernel(const __grid_constant__ Params p, const T *__restrict__ valu
             FwdCell mine = {0, 0, 0.0f, 0.0f, 0.0f, 0.0f};
             const int j = j0 + r;
             if (j < NLP) {
-                const float u = __ldg(lp + j * sJ), v = __ldg(lp + j * sJ + sXY);
-                float A = __ldg(ap + j);
+                const float u = ldl(loc, lo + j * sJ, p.loc_dt), v = ldl(loc, lo + j * sJ + sXY, p.loc_dt);
+                float A = ldl(attn, ao + j, p.loc_dt);
                 if (p.logits) A = expf(A - sm.x) * sm.y;
                 const int l = (int)p.div_p.div((uint32_t)j);
                 const int W = lt.W[l], H = lt.H[l];
@@ -570,12 +597,10 @@ msda_backward_kernel(const __grid_constant__ Params p, const T *__restrict__ gra
         const T *vbh = value + bhoff + r * VEC;
         float *gbh = gv_acc + bhoff + r * VEC;
         const int64_t lrow = rw.b * p.l_sB + (int64_t)((rw.q * (uint32_t)p.N_h + rw.h) * (uint32_t)NLP) * sJ;
-        const float *lp = loc + lrow;
-        float *glp = grad_loc + lrow;
-        const float *ap = attn + (int64_t)rw.bqh * NLP;
-        float *gap = grad_attn + (int64_t)rw.bqh * NLP;
+        const int64_t ao = (int64_t)rw.bqh * NLP;  // row of attention_weights and its gradient
         const bool soft = p.logits && need_a;
-        const float2 sm = soft ? row_softmax_stats<G>(ap, NLP, r, gmask) : make_float2(0.0f, 1.0f);
+        const float2 sm =
+            soft ? row_softmax_stats<G>(attn, ao, NLP, r, gmask, p.loc_dt) : make_float2(0.0f, 1.0f);
         float sAg = 0.0f;  // (logits) this lane's part of sum_j A_j <g, S_j>
         float g[NCH][VEC];
         {
@@ -603,9 +628,9 @@ msda_backward_kernel(const __grid_constant__ Params p, const T *__restrict__ gra
                 float u = 0.0f, v = 0.0f;
                 if (live) {
                     l = (int)p.div_p.div((uint32_t)j);
-                    u = __ldg(lp + j * sJ);
-                    v = __ldg(lp + j * sJ + sXY);
-                    if (need_a) A = __ldg(ap + j);
+                    u = ldl(loc, lrow + j * sJ, p.loc_dt);
+                    v = ldl(loc, lrow + j * sJ + sXY, p.loc_dt);
+                    if (need_a) A = ldl(attn, ao + j, p.loc_dt);
                     if (soft) A = expf(A - sm.x) * sm.y;
                 }
                 const int W = lt.W[l], H = lt.H[l];
@@ -699,11 +724,11 @@ msda_backward_kernel(const __grid_constant__ Params p, const T *__restrict__ gra
                         tx = fmaf(dwx[i], di, tx);
                         ty = fmaf(dwy[i], di, ty);
                     }
-                    if (want_ga) gap[j] = ga;  // (logits: <g, S_j>, turned into d/dlogit below)
+                    if (want_ga) stl(grad_attn, ao + j, ga, p.loc_dt);  // (logits: <g, S_j>, made d/dlogit below)
                     if (soft) sAg = fmaf(A, ga, sAg);
                     if (want_gl) {
-                        glp[j * sJ] = A * tx * (lt.sx[l] * c.kx);
-                        glp[j * sJ + sXY] = A * ty * (lt.sy[l] * c.ky);
+                        stl(grad_loc, lrow + j * sJ, A * tx * (lt.sx[l] * c.kx), p.loc_dt);
+                        stl(grad_loc, lrow + j * sJ + sXY, A * ty * (lt.sy[l] * c.ky), p.loc_dt);
                     }
                 }
             }
@@ -714,8 +739,8 @@ msda_backward_kernel(const __grid_constant__ Params p, const T *__restrict__ gra
 #pragma unroll
             for (int o = G / 2; o >= 1; o >>= 1) sAg += __shfl_xor_sync(gmask, sAg, o);
             for (int j = r; j < NLP; j += G) {
-                const float A = expf(__ldg(ap + j) - sm.x) * sm.y;
-                gap[j] = A * (gap[j] - sAg);
+                const float A = expf(ldl(attn, ao + j, p.loc_dt) - sm.x) * sm.y;
+                stl(grad_attn, ao + j, A * (ldl_own(grad_attn, ao + j, p.loc_dt) - sAg), p.loc_dt);
             }
         }
     }
@@ -762,9 +787,9 @@ msda_count_kernel(const __grid_constant__ Params p, const float *__restrict__ lo
             b[t] = 0;
             if (s < total) {
                 b[t] = s / per_batch;
-                const float *lp = loc + b[t] * p.l_sB + (int64_t)(s - b[t] * per_batch) * p.l_sJ;
-                u[t] = __ldg(lp);
-                v[t] = __ldg(lp + p.l_sXY);
+                const int64_t lo = b[t] * p.l_sB + (int64_t)(s - b[t] * per_batch) * p.l_sJ;
+                u[t] = ldl(loc, lo, p.loc_dt);
+                v[t] = ldl(loc, lo + p.l_sXY, p.loc_dt);
             }
         }
 #pragma unroll

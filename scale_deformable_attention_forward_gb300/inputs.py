@@ -58,6 +58,7 @@ class Workload:
     N_p: int
     levels: Tuple[Tuple[int, int], ...]
     dtype: str = "f32"  # storage dtype of value / out / grad_output / grad_value
+    loc_dtype: str = "f32"  # storage dtype of locations, attention weights / logits and their gradients
     value_layout: str = "BLNC"
     loc_layout: str = "BQHLP2"
     align_corners: bool = False
@@ -144,6 +145,8 @@ def store_dtype(x: np.ndarray, dtype: str) -> np.ndarray:
         return np.ascontiguousarray(x, dtype=np.float32)
     if dtype == "bf16":
         return round_to_bf16(x)
+    if dtype == "f16":
+        return np.ascontiguousarray(np.asarray(x, dtype=np.float64).astype(np.float16), dtype=np.float32)
     raise ValueError(f"unknown dtype {dtype!r}")
 
 
@@ -238,9 +241,9 @@ def generate(w: Workload, seed: Optional[int] = None) -> dict:
 
     return {
         "value": to_value_layout(store_dtype(value, w.dtype), w.value_layout),
-        "sampling_locations": to_loc_layout(store_dtype(loc, "f32"), w.loc_layout),
-        "attention_weights": store_dtype(attn, "f32"),
-        "attention_logits": store_dtype(raw_logits, "f32"),  # the logits the weights come from
+        "sampling_locations": to_loc_layout(store_dtype(loc, w.loc_dtype), w.loc_layout),
+        "attention_weights": store_dtype(attn, w.loc_dtype),
+        "attention_logits": store_dtype(raw_logits, w.loc_dtype),  # the logits the weights come from
         "grad_output": store_dtype(grad_output, w.dtype),
         "spatial_shapes": tuple(tuple(int(x) for x in hw) for hw in w.levels),
         "level_start_index": w.level_start_index,

@@ -90,7 +90,9 @@ def test_rejections_forward(lib):
     assert _fwd(lib, d(DIMS, LEVELS, (0, 23))) == -5          # start[1] != H0*W0
     assert _fwd(lib, d((2, 5, 3, 8, 2, 4, 31), LEVELS, STARTS)) == -5  # L != sum
     assert _fwd(lib, d(DIMS, ((0, 6), (2, 3)), (0, 0))) == -5  # empty level
-    assert _fwd(lib, d(DIMS, LEVELS, STARTS, value_dtype=msda.DTYPE_F32, loc_dtype=1)) == -8
+    assert _fwd(lib, d(DIMS, LEVELS, STARTS, value_dtype=msda.DTYPE_F16)) == -8  # binary16 value
+    assert _fwd(lib, d(DIMS, LEVELS, STARTS, loc_dtype=7)) == -2
+    assert _fwd(lib, d(DIMS, LEVELS, STARTS, loc_dtype=msda.DTYPE_BF16), loc=ctypes.c_void_p(0x10001)) == -9
     assert _fwd(lib, d(DIMS, LEVELS, STARTS), value=ctypes.c_void_p(0x10002)) == -9
     big = ((46341, 46341),)
     assert _fwd(lib, d((1, 1, 1, 1, 1, 1, 46341 * 46341), big, (0,))) == -7

@@ -98,6 +98,16 @@ def test_channel_counts_sorted(dtype, C_h):
     check_workload(w, flag_sets=[(True, False, False)], check_forward=False)
 
 
+@pytest.mark.parametrize("loc_dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("N_q,ll", [(37, "BQHLP2"), (150, "B2QHLP")])  # 150: cell-sorted grad_value too
+def test_16bit_locations(loc_dtype, dtype, N_q, ll):
+    """Locations, weights and their gradients stored in bfloat16 or binary16
+    (arithmetic binary32); the oracle reads the same 16-bit numbers."""
+    w = _small(dtype, "BLNC", ll, False, "zeros", N_q=N_q, seed=31).with_(loc_dtype=loc_dtype)
+    check_workload(w, flag_sets=[(True, True, True), (True, False, False), (False, False, True)])
+
+
 @pytest.mark.parametrize("N_p", [1, 5, 8, 13])
 def test_points_per_level(N_p):
     """N_l*N_p not a multiple of the samples in flight per warp."""
