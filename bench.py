@@ -222,26 +222,69 @@ def cpu_model() -> str:
     return platform.processor() or platform.machine()
 
 
-def time_oracle(w, data, target_s: float):
-    """Time the oracle on a slice sized for about target_s seconds."""
+_WORKER = {}
+
+
+def _oracle_worker_init(workload: str):
+    """Pool initializer: each process builds the same seeded inputs (outside
+    any timing)."""
+    import oracle
+    w = gen.WORKLOADS[workload]
+    _WORKER["w"], _WORKER["data"], _WORKER["orc"] = w, gen.generate(w), oracle.default()
+
+
+def _oracle_worker_run(job):
+    """Forward + backward of queries [q0, q1) of batch item 0, `reps` times
+    (the float64 slice is built once per process and kept)."""
+    q0, q1, reps = job
+    w, data, orc = _WORKER["w"], _WORKER["data"], _WORKER["orc"]
+    key = (q0, q1)
+    if _WORKER.get("key") != key:
+        _WORKER["key"], _WORKER["slice"] = key, oracle_slice(w, data, q0, q1)
+    sub, samples = _WORKER["slice"]
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        oracle_step(orc, w, data, sub)
+    return samples * reps, time.perf_counter() - t0
+
+
+def oracle_slice(w, data, q0, q1):
+    loc = data["sampling_locations"]
+    loc = loc[0:1, q0:q1] if w.loc_layout == "BQHLP2" else loc[0:1, :, q0:q1]
+    sub = {
+        "value": np.ascontiguousarray(data["value"][0:1], dtype=np.float64),
+        "sampling_locations": np.ascontiguousarray(loc, dtype=np.float64),
+        "attention_weights": np.ascontiguousarray(data["attention_weights"][0:1, q0:q1], dtype=np.float64),
+        "grad_output": np.ascontiguousarray(data["grad_output"][0:1, q0:q1], dtype=np.float64),
+    }
+    return sub, (q1 - q0) * w.N_h * w.N_l * w.N_p
+
+
+def time_oracle(w, workload: str, data, target_s: float, cores: int):
+    """The oracle, as it stands, on `cores` host processes (a spawn pool: the
+    parent has already used the GPU), each on its own query slice of batch
+    item 0, for about target_s seconds.  Returns (Gsamples/s, samples, n_q
+    per process, seconds, reps)."""
+    import multiprocessing as mp
     import oracle
     orc = oracle.default()
     probe_q = max(1, min(w.n_queries, 256))
     sub, s = oracle_sample(w, data, probe_q)
     t0 = time.perf_counter()
     oracle_step(orc, w, data, sub)
-    rate = s / max(time.perf_counter() - t0, 1e-6)
-    n_q = int(min(w.n_queries, max(1, target_s * rate / (w.N_h * w.N_l * w.N_p))))
-    sub, samples = oracle_sample(w, data, n_q)
-    reps = 0
-    t0 = time.perf_counter()
-    while True:  # repeat the slice until about target_s of CPU work is done
-        oracle_step(orc, w, data, sub)
-        reps += 1
-        dt = time.perf_counter() - t0
-        if dt >= 0.8 * target_s:
-            break
-    return samples * reps / dt / 1e9, samples, n_q, dt, reps
+    rate = s / max(time.perf_counter() - t0, 1e-6)  # samples/s of one process
+    per_q = w.N_h * w.N_l * w.N_p
+    n_q = int(max(1, min(w.n_queries // cores, target_s * rate / per_q)))
+    reps = max(1, int(target_s * rate / (n_q * per_q)))
+    jobs = [(i * n_q, (i + 1) * n_q, reps) for i in range(cores)]
+    ctx = mp.get_context("spawn")
+    with ctx.Pool(cores, initializer=_oracle_worker_init, initargs=(workload,)) as pool:
+        pool.map(_oracle_worker_run, [(j[0], j[1], 1) for j in jobs])  # workers up, slices built, warm
+        t0 = time.perf_counter()
+        res = pool.map(_oracle_worker_run, jobs)
+        wall = time.perf_counter() - t0
+    samples = sum(r[0] for r in res)
+    return samples / wall / 1e9, samples, n_q, wall, reps
 
 
 # ----------------------------------------------------------------------------- GPU leg
@@ -314,33 +357,63 @@ def run_ours(args, w: gen.Workload):
     step_ms = max_over_ranks(step_ms_local, world, dev)
     value = w.samples * world / (step_ms * 1e-3) / 1e9
 
-    # End to end: pinned host inputs -> device, forward, backward, results -> pinned host.
-    host_out = {"out": torch.empty(out.shape, dtype=vt).pin_memory(),
-                "gv": torch.empty(gv.shape, dtype=vt).pin_memory(),
-                "gl": torch.empty(gl.shape, dtype=torch.float32).pin_memory(),
-                "ga": torch.empty(ga.shape, dtype=torch.float32).pin_memory()}
+    # End to end: pinned host inputs -> device, forward, backward, results ->
+    # pinned host, every step.  Two buffer sets and three streams pipeline the
+    # steps the way a production loop would: the inputs of step i+1 are copied
+    # in and the results of step i-1 copied out while step i computes.
     h2d = sum(v.numel() * v.element_size() for v in host.values())
-    d2h = sum(v.numel() * v.element_size() for v in host_out.values())
+    outs_shape = {"out": (out.shape, vt), "gv": (gv.shape, vt), "gl": (gl.shape, torch.float32),
+                  "ga": (ga.shape, torch.float32)}
+    host_out = [{k: torch.empty(s, dtype=dt).pin_memory() for k, (s, dt) in outs_shape.items()} for _ in range(2)]
+    d2h = sum(v.numel() * v.element_size() for v in host_out[0].values())
+    dev_in = [t] + [{k: torch.empty_like(v) for k, v in t.items()}]
+    dev_out = [{"out": out, "gv": gv, "gl": gl, "ga": ga},
+               {"out": torch.empty_like(out), "gv": torch.empty_like(gv), "gl": torch.empty_like(gl),
+                "ga": torch.empty_like(ga)}]
+    s_in, s_comp, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_comp = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+    for e in ev_comp + ev_out:
+        e.record(stream)
     K_e2e = max(3, min(K, 200))
 
-    def e2e_step():
-        for k in host:
-            t[k].copy_(host[k], non_blocking=True)
-        fwd()
-        bwd()
-        host_out["out"].copy_(out, non_blocking=True)
-        host_out["gv"].copy_(gv, non_blocking=True)
-        host_out["gl"].copy_(gl, non_blocking=True)
-        host_out["ga"].copy_(ga, non_blocking=True)
+    def e2e_step(i):
+        k = i % 2
+        di, do = dev_in[k], dev_out[k]
+        with torch.cuda.stream(s_in):  # inputs of step i (buffer k's last reader: step i-2's compute)
+            s_in.wait_event(ev_comp[k])
+            for name in host:
+                di[name].copy_(host[name], non_blocking=True)
+            ev_in[k].record(s_in)
+        with torch.cuda.stream(s_comp):  # compute (buffer k's outputs copied out by step i-2 first)
+            s_comp.wait_event(ev_in[k])
+            s_comp.wait_event(ev_out[k])
+            msda.msda_forward(di["value"], data["spatial_shapes"], data["level_start_index"],
+                              di["sampling_locations"], di["attention_weights"], out=do["out"], **kw)
+            msda.msda_backward(di["grad_output"], di["value"], data["spatial_shapes"], data["level_start_index"],
+                               di["sampling_locations"], di["attention_weights"], grad_value=do["gv"],
+                               grad_sampling_locations=do["gl"], grad_attention_weights=do["ga"], workspace=ws,
+                               **kw)
+            ev_comp[k].record(s_comp)
+        with torch.cuda.stream(s_out):  # results of step i
+            s_out.wait_event(ev_comp[k])
+            for name in host_out[k]:
+                host_out[k][name].copy_(do[name], non_blocking=True)
+            ev_out[k].record(s_out)
 
-    for _ in range(3):
-        e2e_step()
+    for i in range(3):
+        e2e_step(i)
     torch.cuda.synchronize(dev)
     barrier(world)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(K_e2e):
-        e2e_step()
+    for st in (s_in, s_comp, s_out):
+        st.wait_event(e0)
+    for i in range(K_e2e):
+        e2e_step(i)
+    for st in (s_in, s_comp, s_out):
+        stream.wait_stream(st)
     e1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / K_e2e, world, dev)
@@ -378,7 +451,9 @@ def run_ours(args, w: gen.Workload):
         "clocks": clk.summary(),
         "e2e": {"value": round(w.samples * world / (e2e_ms * 1e-3) / 1e9, 4), "unit": UNIT,
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "path": "pinned host -> device copies, msda_forward, msda_backward, device -> pinned host"},
+                "path": "per step: pinned host -> device copies of the inputs, msda_forward, msda_backward, "
+                        "device -> pinned host copies of all four results; double-buffered on three streams "
+                        "(copies of neighbouring steps overlap the compute)"},
         "gpu_launches": launches_per_step * K,
         "roofline": {
             "kernel": dominant + (" (zero-fill + fused gather/scatter kernel)" if dominant == "msda_backward"
@@ -396,11 +471,13 @@ def run_ours(args, w: gen.Workload):
         },
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v, samples, n_q, dt, reps = time_oracle(w, data, args.cpu_seconds)
+        cores = max(1, os.cpu_count() or 1)
+        v, samples, n_q, dt, reps = time_oracle(w, args.workload, data, args.cpu_seconds, cores)
         result["cpu_baseline"] = {
-            "value": round(v, 6), "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"batch item 0, queries [0,{n_q}) of {w.n_queries}, all heads/levels/points "
-                      f"({samples} samples), forward + backward x{reps}, float64, {dt:.1f} s",
+            "value": round(v, 6), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"batch item 0: {cores} processes, each queries [{n_q}*i, {n_q}*(i+1)) of {w.n_queries} "
+                      f"with all heads/levels/points, forward + backward x{reps} in float64; {samples} samples "
+                      f"in {dt:.1f} s wall",
             "cpu": cpu_model()}
     if rank == 0:
         print(json.dumps(result), flush=True)
@@ -410,13 +487,16 @@ def run_ours(args, w: gen.Workload):
 
 
 def run_reference(args, w: gen.Workload):
-    """The oracle on the host cores, on a bounded slice per step."""
+    """The oracle on all host cores (a spawn pool, one query slice per
+    process), a bounded slice of the workload per step."""
+    import multiprocessing as mp
     world, rank, _ = dist_setup()
     if rank != 0:
         return
     import oracle
     orc = oracle.default()
     data = gen.generate(w)
+    cores = max(1, os.cpu_count() or 1)
     total_steps = args.warmup + args.steps
     per_step_s = max(0.005, args.reference_seconds / max(1, total_steps))
     probe_q = max(1, min(w.n_queries, 64))
@@ -424,24 +504,29 @@ def run_reference(args, w: gen.Workload):
     t0 = time.perf_counter()
     oracle_step(orc, w, data, sub)
     rate = s / max(time.perf_counter() - t0, 1e-6)
-    n_q = int(min(w.n_queries, max(1, per_step_s * rate / (w.N_h * w.N_l * w.N_p))))
-    sub, samples = oracle_sample(w, data, n_q)
-    for _ in range(args.warmup):
-        oracle_step(orc, w, data, sub)
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        oracle_step(orc, w, data, sub)
-    dt = time.perf_counter() - t0
-    value = samples * args.steps / dt / 1e9
+    per_q = w.N_h * w.N_l * w.N_p
+    n_q = int(min(max(1, w.n_queries // cores), max(1, per_step_s * rate / per_q)))
+    jobs = [(i * n_q, (i + 1) * n_q, 1) for i in range(cores)]
+    ctx = mp.get_context("spawn")
+    with ctx.Pool(cores, initializer=_oracle_worker_init, initargs=(args.workload,)) as pool:
+        for _ in range(args.warmup):
+            pool.map(_oracle_worker_run, jobs)
+        t0 = time.perf_counter()
+        done = 0
+        for _ in range(args.steps):
+            done += sum(r[0] for r in pool.map(_oracle_worker_run, jobs))
+        dt = time.perf_counter() - t0
+    value = done / dt / 1e9
     result = {
         "impl": "reference",
         "metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded Deformable-DETR-shaped inputs)",
         "config": {"workload": gen.WORKLOAD_DESCRIPTIONS.get(args.workload, args.workload), "name": args.workload},
-        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "kind": "oracle", "cores": 1,
-                         "sample": f"per step: batch item 0, queries [0,{n_q}) of {w.n_queries}, all "
-                                   f"heads/levels/points ({samples} samples), forward + backward, float64",
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "kind": "oracle", "cores": cores,
+                         "sample": f"per step: batch item 0, {cores} processes each on {n_q} queries "
+                                   f"(all heads/levels/points; {cores * n_q * per_q} samples), forward + "
+                                   f"backward, float64",
                          "cpu": cpu_model()},
         "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "note": "no GPU implementation exists for this operator on the reference pages; the reference arm "

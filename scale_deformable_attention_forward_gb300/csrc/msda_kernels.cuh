@@ -414,9 +414,12 @@ __device__ __forceinline__ FwdCell fwd_cell(const Cell &c, float A, int W, int H
 // walks the G samples, receiving each cell from its owner by shuffles, and
 // loads every corner's channel row with one instruction per channel chunk
 // (lane r owns chunks r, r+G, ...), two samples' corners in flight.
-// PAD: 0 zeros, 1 border, -1 read p.padding at run time.
-template <typename T, int VEC, int G, int NCH, int PAD>
-__global__ void __launch_bounds__(kThreads, row_min_blocks(NCH *VEC, true))
+// PAD: 0 zeros, 1 border, -1 read p.padding at run time.  GEN: false for
+// binary32 weights (p.loc_dt == 0, p.logits == 0, the common case compiled
+// without the branches), true reads both at run time (with the backward's
+// register budget: the softmax statistics need registers).
+template <typename T, int VEC, int G, int NCH, int PAD, bool GEN>
+__global__ void __launch_bounds__(kThreads, row_min_blocks(NCH *VEC, !GEN))
 msda_forward_kernel(const __grid_constant__ Params p, const T *__restrict__ value, const float *__restrict__ loc,
                     const float *__restrict__ attn, T *__restrict__ out) {
     __shared__ LevelTables lt;
@@ -437,8 +440,9 @@ msda_forward_kernel(const __grid_constant__ Params p, const T *__restrict__ valu
         const T *vbh = value + rw.b * p.v_sB + (int64_t)rw.h * p.v_sH + r * VEC;
         const int64_t lo = rw.b * p.l_sB + (int64_t)((rw.q * (uint32_t)p.N_h + rw.h) * (uint32_t)NLP) * sJ;
         const int64_t ao = (int64_t)rw.bqh * NLP;
-        const float2 sm =
-            p.logits ? row_softmax_stats<G>(attn, ao, NLP, r, gmask, p.loc_dt) : make_float2(0.0f, 1.0f);
+        const int ldt = GEN ? p.loc_dt : 0;
+        const bool logits = GEN && p.logits;
+        const float2 sm = logits ? row_softmax_stats<G>(attn, ao, NLP, r, gmask, ldt) : make_float2(0.0f, 1.0f);
 
         float acc[NCH][VEC];
 #pragma unroll
@@ -451,9 +455,9 @@ msda_forward_kernel(const __grid_constant__ Params p, const T *__restrict__ valu
             FwdCell mine = {0, 0, 0.0f, 0.0f, 0.0f, 0.0f};
             const int j = j0 + r;
             if (j < NLP) {
-                const float u = ldl(loc, lo + j * sJ, p.loc_dt), v = ldl(loc, lo + j * sJ + sXY, p.loc_dt);
-                float A = ldl(attn, ao + j, p.loc_dt);
-                if (p.logits) A = expf(A - sm.x) * sm.y;
+                const float u = ldl(loc, lo + j * sJ, ldt), v = ldl(loc, lo + j * sJ + sXY, ldt);
+                float A = ldl(attn, ao + j, ldt);
+                if (logits) A = expf(A - sm.x) * sm.y;
                 const int l = (int)p.div_p.div((uint32_t)j);
                 const int W = lt.W[l], H = lt.H[l];
                 const Cell c = make_cell<PAD>(u, v, lt.sx[l], lt.sy[l], p.off, W, H, p.padding);

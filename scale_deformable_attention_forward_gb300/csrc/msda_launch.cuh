@@ -33,10 +33,10 @@ unsigned row_grid(K kernel, int G, const Params &p) {
     return (unsigned)blocks;
 }
 
-template <typename T, int V, int GG, int NN, int PAD>
+template <typename T, int V, int GG, int NN, int PAD, bool GEN>
 cudaError_t fwd_launch(const Params &p, const T *value, const float *loc, const float *attn, T *out,
                        cudaStream_t stream) {
-    auto kernel = msda_forward_kernel<T, V, GG, NN, PAD>;
+    auto kernel = msda_forward_kernel<T, V, GG, NN, PAD, GEN>;
     const unsigned blocks = row_grid(kernel, GG, p);
     kernel<<<blocks, kThreads, 0, stream>>>(p, value, loc, attn, out);
     return cudaGetLastError();
@@ -46,10 +46,14 @@ template <typename T, int V, int GG, int NN>
 cudaError_t fwd_shape(const Params &p, const T *value, const float *loc, const float *attn, T *out,
                       cudaStream_t stream) {
     if constexpr (V > 1 && specialised_shape(GG, NN)) {
-        if (p.padding == 0) return fwd_launch<T, V, GG, NN, 0>(p, value, loc, attn, out, stream);
-        return fwd_launch<T, V, GG, NN, 1>(p, value, loc, attn, out, stream);
+        const bool gen = p.loc_dt != 0 || p.logits != 0;
+        if (p.padding == 0)
+            return gen ? fwd_launch<T, V, GG, NN, 0, true>(p, value, loc, attn, out, stream)
+                       : fwd_launch<T, V, GG, NN, 0, false>(p, value, loc, attn, out, stream);
+        return gen ? fwd_launch<T, V, GG, NN, 1, true>(p, value, loc, attn, out, stream)
+                   : fwd_launch<T, V, GG, NN, 1, false>(p, value, loc, attn, out, stream);
     } else {
-        return fwd_launch<T, V, GG, NN, -1>(p, value, loc, attn, out, stream);
+        return fwd_launch<T, V, GG, NN, -1, true>(p, value, loc, attn, out, stream);
     }
 }
 
