@@ -42,6 +42,7 @@ from scale_deformable_attention_forward_gb300 import inputs as gen  # noqa: E402
 METRIC = "MSDA fwd+bwd Gsamples/s (q·h·l·p) and achieved HBM GB/s vs GB300 peak"
 UNIT = "Gsamples/s"
 FALLBACK_HBM_GBS = 6800.0
+REDUCTION_GBS = 6710.0  # measured binary32 red.global.add payload rate of a GB300
 CSRC = os.path.join(ROOT, "scale_deformable_attention_forward_gb300", "csrc")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")
 
@@ -463,6 +464,15 @@ def run_ours(args, w: gen.Workload):
             "algorithmic_bytes_per_launch": dom_bytes,
             "traffic": (traffic or {}).get(dominant),
         },
+        # The backward's real bound: the binary32 reductions of grad_value (four corner rows of
+        # C_h values per sample), against the reduction rate a microbenchmark of red.global.add
+        # measured on this GPU (6.7 TB/s of payload, whatever the request shape).
+        "roofline_reduction": {
+            "what": "grad_value reduction payload (samples x 4 corners x C_h x 4 B) / backward time",
+            "achieved": round(w.samples * 4 * w.C_h * 4 / (bwd_mean * 1e-3) / 1e9, 1),
+            "peak": REDUCTION_GBS, "unit": "GB/s",
+            "frac": round(w.samples * 4 * w.C_h * 4 / (bwd_mean * 1e-3) / 1e9 / REDUCTION_GBS, 4),
+            "peak_source": "red.global.add.v4.f32 microbenchmark on GB300 (random 128-byte lines)"},
         "roofline_step": {
             "what": "forward + backward compulsory bytes / step time",
             "achieved": round((fwd_b + bwd_b) / (step_ms * 1e-3) / 1e9, 1), "peak": peak, "unit": "GB/s",
