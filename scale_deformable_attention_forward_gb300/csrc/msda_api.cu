@@ -97,6 +97,38 @@ msda::FastDiv make_fastdiv(uint32_t d) {
     return f;
 }
 
+// Tile partition of the tile-sorted grad_value (see msda_kernels.cuh): per
+// level, ceil((H+1)/T) x ceil((W+1)/T) tiles of T x T cells; partition blocks
+// of part_rows (about 512) rows each, at most 1024 of them; `usable` when the
+// sizes fit the kernels' 32-bit indices and shared-memory tables.
+struct TileGeom {
+    int64_t NB, bst[msda::kMaxLevels], BX[msda::kMaxLevels];
+    int64_t nbins, parts, part_rows, span;
+    bool usable;
+};
+
+TileGeom tile_geom(const msda_desc *d) {
+    TileGeom g;
+    memset(&g, 0, sizeof(g));
+    const int64_t T = msda::kTileCells;
+    for (int64_t l = 0; l < d->N_l; ++l) {
+        const int64_t H = d->spatial_shapes[2 * l], W = d->spatial_shapes[2 * l + 1];
+        g.bst[l] = g.NB;
+        g.BX[l] = (W + 1 + T - 1) / T;
+        g.NB += ((H + 1 + T - 1) / T) * g.BX[l];
+    }
+    const int64_t rows = d->B * d->N_h * d->N_q;
+    const int64_t samples = rows * d->N_l * d->N_p;
+    g.nbins = d->B * d->N_h * g.NB;
+    g.parts = rows > 0 ? (rows + 511) / 512 : 1;
+    if (g.parts > 1024) g.parts = 1024;
+    g.part_rows = rows > 0 ? (rows + g.parts - 1) / g.parts : 1;
+    g.span = d->N_q > 0 ? (g.part_rows + d->N_q - 1) / d->N_q + 1 : 1;
+    g.usable = rows > 0 && samples < (int64_t)INT32_MAX && rows < ((int64_t)1 << msda::kEntryCellShift) &&
+               g.nbins * g.parts + 1 < (int64_t)INT32_MAX && g.span * g.NB * 4 <= 48 * 1024;
+    return g;
+}
+
 Params make_params(const msda_desc *d, const Config &cfg, int V_vec) {
     Params p;
     memset(&p, 0, sizeof(p));
@@ -145,33 +177,16 @@ Params make_params(const msda_desc *d, const Config &cfg, int V_vec) {
         p.sy[l] = (float)(d->align_corners ? H - 1 : H);
     }
     p.off = d->align_corners ? 0.0f : -0.5f;
-    // cell keys: (H_l + 1) x (W_l + 1) per level and (b, h); the reduction
-    // takes the levels with the fewest pixels (longest lists) first
-    int64_t K = 0;
-    for (int64_t l = 0; l < d->N_l; ++l) {
-        p.kst[l] = (int)K;
-        K += (d->spatial_shapes[2 * l] + 1) * (d->spatial_shapes[2 * l + 1] + 1);
+    const TileGeom tg = tile_geom(d);
+    p.NB = (int)tg.NB;
+    for (int l = 0; l < (int)d->N_l; ++l) {
+        p.bst[l] = (int)tg.bst[l];
+        p.BX[l] = (int)tg.BX[l];
     }
-    // (used only by the cell-sorted grad_value, which plan_backward allows
-    // only when nkeys fits in 31 bits)
-    p.K_bh = K < INT32_MAX ? (int)K : 0;
-    p.nkeys = d->B * d->N_h * K < INT32_MAX ? (uint32_t)(d->B * d->N_h * K) : 0u;
-    int order[msda::kMaxLevels];
-    for (int l = 0; l < (int)d->N_l; ++l) order[l] = l;
-    for (int a = 1; a < (int)d->N_l; ++a)
-        for (int b = a; b > 0 && (int64_t)p.H[order[b]] * p.W[order[b]] < (int64_t)p.H[order[b - 1]] * p.W[order[b - 1]];
-             --b) {
-            const int t = order[b];
-            order[b] = order[b - 1];
-            order[b - 1] = t;
-        }
-    uint32_t end = 0;
-    for (int i = 0; i < (int)d->N_l; ++i) {
-        const int l = order[i];
-        p.ilev[i] = l;
-        end += (uint32_t)(d->B * d->N_h * (int64_t)(p.H[l] + 1) * (p.W[l] + 1));
-        p.iend[i] = end;
-    }
+    p.nbins = tg.usable ? (uint32_t)tg.nbins : 0u;
+    p.parts = (uint32_t)tg.parts;
+    p.part_rows = (uint32_t)tg.part_rows;
+    p.span = (int)tg.span;
     p.capacity = (uint32_t)(d->B * d->N_q * d->N_h * d->N_l * d->N_p);
     return p;
 }
@@ -189,23 +204,22 @@ int sm_count() {
 
 // Workspace of the backward, in 256-byte aligned regions:
 //   acc      binary32 grad_value accumulator (bfloat16 value with grad_value)
-//   offsets  cell-key counts, then offsets (nkeys + 1 int32)   \
-//   cursor   append positions (nkeys int32)                     |  cell-sorted
-//   tiles    tile sums of the scan                              |  grad_value
-//   entries  the samples grouped by cell (samples x 16 bytes)  /
-// The cell-sorted regions are planned when there are at least
-// MSDA_SORT_MIN_DENSITY samples per cell key on average (below that the
-// count, scan and per-key pass cost more than the atomics they save) and the
-// 32-bit entry indices cover the samples.  They are used when grad_value is
-// the only output: next to the value gather of the other two gradients, the
-// sort's own scattered atomics (one count and one append per sample) cost
-// more than the direct per-corner atomics they replace.
+//   offsets  (tile, part) counts, then offsets (nbins * parts + 1 int32)  \
+//   chunks   per-tile chunk counts, then chunk offsets (nbins + 1)        |  tile-sorted
+//   tiles    tile sums of the scans                                      |  grad_value
+//   entries  the samples grouped by tile (samples x 16 bytes)            /
+// The tile-sorted grad_value is used when grad_value is the only output, there
+// are at least MSDA_SORT_MIN_DENSITY samples per bilinear cell on average
+// (below that its partition passes cost more than the atomics they save), the
+// vector path applies (C_h a multiple of 4) and the tile geometry is usable;
+// its regions are planned whenever grad_value is requested (the workspace size
+// depends on the descriptor only).
 #ifndef MSDA_SORT_MIN_DENSITY
 #define MSDA_SORT_MIN_DENSITY 2
 #endif
 struct BwdPlan {
     bool sort;
-    size_t acc_off, offsets_off, cursor_off, tiles_off, entries_off, total;
+    size_t acc_off, offsets_off, chunks_off, tiles_off, entries_off, total;
 };
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -215,23 +229,24 @@ BwdPlan plan_backward(const msda_desc *d, int compute_grad_value, bool allow_sor
     memset(&w, 0, sizeof(w));
     if (!compute_grad_value) return w;
     const int64_t samples = d->B * d->N_q * d->N_h * d->N_l * d->N_p;
-    int64_t K = 0;
-    for (int64_t l = 0; l < d->N_l; ++l) K += (d->spatial_shapes[2 * l] + 1) * (d->spatial_shapes[2 * l + 1] + 1);
-    const int64_t nkeys = d->B * d->N_h * K;
-    w.sort = allow_sort && samples > 0 && samples >= (int64_t)MSDA_SORT_MIN_DENSITY * nkeys &&
-             samples < (int64_t)INT32_MAX &&
-             nkeys + 1 < (int64_t)INT32_MAX;
+    int64_t cells = 0;
+    for (int64_t l = 0; l < d->N_l; ++l) cells += (d->spatial_shapes[2 * l] + 1) * (d->spatial_shapes[2 * l + 1] + 1);
+    cells *= d->B * d->N_h;
+    const TileGeom tg = tile_geom(d);
+    w.sort = allow_sort && samples > 0 && samples >= (int64_t)MSDA_SORT_MIN_DENSITY * cells && tg.usable &&
+             d->C_h % 4 == 0;
     size_t end = 0;  // end of the regions so far (each region starts 256-byte aligned)
     if (d->value_dtype == MSDA_DTYPE_BF16) {
         w.acc_off = 0;
         end = (size_t)(d->B * d->L * d->N_h * d->C_h) * sizeof(float);
     }
     if (w.sort) {
-        const int64_t tiles = (nkeys + msda::kScanTile - 1) / msda::kScanTile;
+        const int64_t n = tg.nbins * tg.parts;
+        const int64_t tiles = (n + 1 + msda::kScanTile - 1) / msda::kScanTile;
         w.offsets_off = align256(end);
-        w.cursor_off = align256(w.offsets_off + (size_t)(nkeys + 1) * sizeof(int));
-        w.tiles_off = align256(w.cursor_off + (size_t)nkeys * sizeof(int));
-        w.entries_off = align256(w.tiles_off + (size_t)(tiles > 0 ? tiles : 1) * sizeof(int));
+        w.chunks_off = align256(w.offsets_off + (size_t)(n + 1) * sizeof(int));
+        w.tiles_off = align256(w.chunks_off + (size_t)(tg.nbins + 1) * sizeof(int));
+        w.entries_off = align256(w.tiles_off + (size_t)tiles * sizeof(int));
         end = w.entries_off + (size_t)samples * 16;
     }
     w.total = end;
@@ -321,8 +336,7 @@ msda_scan_tiles_kernel(const int *__restrict__ counts, uint32_t n, int *__restri
 }
 
 __global__ void __launch_bounds__(kScanThreads)
-msda_scan_apply_kernel(int *__restrict__ offsets, uint32_t n, const int *__restrict__ tile_sums,
-                       int *__restrict__ cursor) {
+msda_scan_apply_kernel(int *__restrict__ offsets, uint32_t n, const int *__restrict__ tile_sums) {
     __shared__ int warp_sums[32];
     __shared__ int total;
     __shared__ int prefix;
@@ -355,10 +369,7 @@ msda_scan_apply_kernel(int *__restrict__ offsets, uint32_t n, const int *__restr
     int run = ex;
 #pragma unroll
     for (int i = 0; i < kScanPer; ++i) {
-        if (base + i < n) {
-            offsets[base + i] = run;
-            cursor[base + i] = run;
-        }
+        if (base + i < n) offsets[base + i] = run;
         run += v[i];
     }
     if (blockIdx.x == gridDim.x - 1 && threadIdx.x == 0) offsets[n] = prefix + total;
@@ -384,30 +395,52 @@ cudaError_t launch_f32_to_bf16(const float *acc, __nv_bfloat16 *out, int64_t n, 
     return cudaGetLastError();
 }
 
-cudaError_t launch_sort_keys(const Params &p, const float *loc, const BwdBuffers &bb, cudaStream_t stream) {
-    if (p.nkeys == 0) return cudaSuccess;
-    cudaError_t e = launch_zero_f32(reinterpret_cast<float *>(bb.offsets), (int64_t)p.nkeys + 1, stream);
+__global__ void msda_tile_items_kernel(const __grid_constant__ Params p, const int *__restrict__ offsets,
+                                       int *__restrict__ chunks) {
+    const uint32_t tile = blockIdx.x * blockDim.x + threadIdx.x;
+    if (tile >= p.nbins) return;
+    const int beg = offsets[(size_t)tile * p.parts], end = offsets[(size_t)(tile + 1) * p.parts];
+    chunks[tile] = (end - beg + kChunk - 1) / kChunk;
+}
+
+// Exclusive scan of n int32 in place; data[n] = total.
+static cudaError_t launch_scan(int *data, uint32_t n, int *tile_sums, cudaStream_t stream) {
+    const unsigned tiles = (unsigned)(((uint64_t)n + kScanTile - 1) / kScanTile);
+    if (tiles == 0) return cudaSuccess;
+    msda_scan_tiles_kernel<<<tiles, kScanThreads, 0, stream>>>(data, n, tile_sums);
+    cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    const uint64_t samples = (uint64_t)p.rows * (uint64_t)p.NLP;
-    if (samples > 0) {
-        uint64_t blocks = (samples + 1023) / 1024;  // 4 samples a thread
-        const uint64_t cap = (uint64_t)(p.n_sm > 0 ? p.n_sm : 152) * 8;  // grid-stride beyond a few waves
-        if (blocks > cap) blocks = cap;
-        if (p.padding == 0)
-            msda_count_kernel<0><<<(unsigned)blocks, 256, 0, stream>>>(p, loc, bb.offsets);
-        else
-            msda_count_kernel<1><<<(unsigned)blocks, 256, 0, stream>>>(p, loc, bb.offsets);
-        e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
-    }
-    const unsigned tiles = (unsigned)(((uint64_t)p.nkeys + kScanTile - 1) / kScanTile);
-    msda_scan_tiles_kernel<<<tiles, kScanThreads, 0, stream>>>(bb.offsets, p.nkeys, bb.tile_sums);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    msda_scan_apply_kernel<<<tiles, kScanThreads, 0, stream>>>(bb.offsets, p.nkeys, bb.tile_sums, bb.cursor);
+    msda_scan_apply_kernel<<<tiles, kScanThreads, 0, stream>>>(data, n, tile_sums);
     return cudaGetLastError();
 }
 
+cudaError_t launch_tile_partition(const Params &p, const float *loc, const float *attn, const BwdBuffers &bb,
+                                  cudaStream_t stream) {
+    if (p.nbins == 0 || p.rows == 0) return cudaSuccess;
+    const uint32_t n = p.nbins * p.parts;
+    cudaError_t e = launch_zero_f32(reinterpret_cast<float *>(bb.offsets), (int64_t)n + 1, stream);
+    if (e != cudaSuccess) return e;
+    const size_t hist = (size_t)p.span * p.NB * sizeof(int);
+    const unsigned parts = (unsigned)((p.rows + p.part_rows - 1) / p.part_rows);
+    if (p.padding == 0)
+        msda_tile_count_kernel<0><<<parts, 256, hist, stream>>>(p, loc, bb.offsets);
+    else
+        msda_tile_count_kernel<1><<<parts, 256, hist, stream>>>(p, loc, bb.offsets);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    e = launch_scan(bb.offsets, n, bb.tile_sums, stream);
+    if (e != cudaSuccess) return e;
+    msda_tile_items_kernel<<<(p.nbins + 255) / 256, 256, 0, stream>>>(p, bb.offsets, bb.chunks);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    e = launch_scan(bb.chunks, p.nbins, bb.tile_sums, stream);
+    if (e != cudaSuccess) return e;
+    if (p.padding == 0)
+        msda_tile_append_kernel<0><<<parts, 256, hist, stream>>>(p, loc, attn, bb.offsets, bb.entries);
+    else
+        msda_tile_append_kernel<1><<<parts, 256, hist, stream>>>(p, loc, attn, bb.offsets, bb.entries);
+    return cudaGetLastError();
+}
 
 size_t backward_workspace_bytes(const msda_desc *desc, int compute_grad_value, bool allow_sort) {
     if (validate_desc(desc) != MSDA_OK) return 0;
@@ -460,7 +493,7 @@ int backward_entry(const msda_desc *desc, const void *grad_output, const void *v
     bb.grad_attn = (float *)grad_attention_weights;
     if (plan.sort) {
         bb.offsets = (int *)(ws + plan.offsets_off);
-        bb.cursor = (int *)(ws + plan.cursor_off);
+        bb.chunks = (int *)(ws + plan.chunks_off);
         bb.tile_sums = (int *)(ws + plan.tiles_off);
         bb.entries = (uint4 *)(ws + plan.entries_off);
     }
@@ -477,28 +510,29 @@ int backward_entry(const msda_desc *desc, const void *grad_output, const void *v
 
     cudaError_t e = cudaSuccess;
     if (fv && !accumulate) e = launch_zero_f32(bb.gv_acc, value_elems, stream);
-    const bool sort = plan.sort && !fl && !fa;
-    if (e == cudaSuccess && samples > 0 && sort) e = launch_sort_keys(p, (const float *)sampling_locations, bb, stream);
-    if (e == cudaSuccess && samples > 0) {
+    // tile-sorted grad_value (vector path): partition, the row kernel for the
+    // other two gradients only, then the per-tile reduction
+    const bool sort = plan.sort && cfg.vec && !fl && !fa;
+    if (e == cudaSuccess && samples > 0 && sort)
+        e = launch_tile_partition(p, (const float *)sampling_locations, (const float *)attention_weights, bb, stream);
+    Params prow = p;
+    if (sort) prow.flags &= ~kGradValue;
+    if (e == cudaSuccess && samples > 0 && prow.flags) {
         if (bf16)
-            e = launch_backward<__nv_bfloat16>(p, cfg.vec, cfg.G, cfg.NCH, sort,
-                                               (const __nv_bfloat16 *)grad_output, (const __nv_bfloat16 *)value,
-                                               (const float *)sampling_locations, (const float *)attention_weights,
-                                               bb, stream);
+            e = launch_backward<__nv_bfloat16>(prow, cfg.vec, cfg.G, cfg.NCH, (const __nv_bfloat16 *)grad_output,
+                                               (const __nv_bfloat16 *)value, (const float *)sampling_locations,
+                                               (const float *)attention_weights, bb, stream);
         else
-            e = launch_backward<float>(p, cfg.vec, cfg.G, cfg.NCH, sort, (const float *)grad_output,
+            e = launch_backward<float>(prow, cfg.vec, cfg.G, cfg.NCH, (const float *)grad_output,
                                        (const float *)value, (const float *)sampling_locations,
                                        (const float *)attention_weights, bb, stream);
     }
     if (e == cudaSuccess && samples > 0 && sort) {
         if (bf16)
-            e = cfg.vec ? launch_gv_reduce<__nv_bfloat16, true>(p, cfg.G, cfg.NCH,
-                                                                (const __nv_bfloat16 *)grad_output, bb, stream)
-                        : launch_gv_reduce<__nv_bfloat16, false>(p, cfg.G, cfg.NCH,
-                                                                 (const __nv_bfloat16 *)grad_output, bb, stream);
+            e = launch_tile_reduce<__nv_bfloat16, true>(p, cfg.G, cfg.NCH, (const __nv_bfloat16 *)grad_output, bb,
+                                                        stream);
         else
-            e = cfg.vec ? launch_gv_reduce<float, true>(p, cfg.G, cfg.NCH, (const float *)grad_output, bb, stream)
-                        : launch_gv_reduce<float, false>(p, cfg.G, cfg.NCH, (const float *)grad_output, bb, stream);
+            e = launch_tile_reduce<float, true>(p, cfg.G, cfg.NCH, (const float *)grad_output, bb, stream);
     }
     if (e == cudaSuccess && fv && bf16 && !accumulate) e = launch_f32_to_bf16(bb.gv_acc, (__nv_bfloat16 *)grad_value, value_elems, stream);
     return record_cuda(e);

@@ -2,7 +2,7 @@
 #include "msda_launch.cuh"
 
 namespace msda {
-template cudaError_t launch_backward_pad<__nv_bfloat16, 1>(const Params &, int, int, bool, const __nv_bfloat16 *,
+template cudaError_t launch_backward_pad<__nv_bfloat16, 1>(const Params &, int, int, const __nv_bfloat16 *,
                                                           const __nv_bfloat16 *, const float *, const float *,
                                                           const BwdBuffers &, cudaStream_t);
 }  // namespace msda

@@ -2,7 +2,7 @@
 #include "msda_launch.cuh"
 
 namespace msda {
-template cudaError_t launch_backward_pad<float, -2>(const Params &, int, int, bool, const float *,
+template cudaError_t launch_backward_pad<float, -2>(const Params &, int, int, const float *,
                                                           const float *, const float *, const float *,
                                                           const BwdBuffers &, cudaStream_t);
 }  // namespace msda

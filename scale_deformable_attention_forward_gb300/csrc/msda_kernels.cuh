@@ -68,13 +68,15 @@ struct Params {
     float sx[kMaxLevels], sy[kMaxLevels];  // pixels per unit of normalised coordinate
     float off;                             // -0.5 (align_corners = 0) or 0 (align_corners = 1)
     int n_sm;                              // multiprocessors of the device (grid sizing)
-    // cell-sorted grad_value (see the sorting kernels below)
-    int K_bh;                   // cell keys of one (b, h): sum over levels of (H_l + 1) * (W_l + 1)
-    int kst[kMaxLevels];        // first key of level l inside a (b, h)
-    uint32_t nkeys;             // B * N_h * K_bh
+    // tile-sorted grad_value (see the partition and reduction kernels below)
+    int NB;                     // tiles (kTileCells x kTileCells cells) of one (b, h)
+    int bst[kMaxLevels];        // first tile of level l inside a (b, h)
+    int BX[kMaxLevels];         // tiles per tile row of level l
+    uint32_t nbins;             // B * N_h * NB
+    uint32_t parts;             // partition blocks (counts are kept per tile and block)
+    uint32_t part_rows;         // rows of one partition block
+    int span;                   // most (b, h) pairs one partition block's rows touch
     uint32_t capacity;          // entries the workspace holds (= samples)
-    int ilev[kMaxLevels];       // reduction order of the levels (fewest pixels first)
-    uint32_t iend[kMaxLevels];  // running end of the reduction's keys, per position in that order
 };
 
 enum : int { kGradValue = 1, kGradLoc = 2, kGradAttn = 4 };
@@ -268,7 +270,7 @@ __device__ __forceinline__ Cell make_cell(float u, float v, float sx, float sy, 
 // Level tables copied to shared memory once per block: the lanes of a warp
 // look up different levels at once, which shared memory serves in one pass.
 struct LevelTables {
-    int W[kMaxLevels], H[kMaxLevels], start[kMaxLevels], kst[kMaxLevels];
+    int W[kMaxLevels], H[kMaxLevels], start[kMaxLevels], bst[kMaxLevels], BX[kMaxLevels];
     float sx[kMaxLevels], sy[kMaxLevels];
 };
 __device__ __forceinline__ void load_level_tables(const Params &p, LevelTables &t) {
@@ -277,7 +279,8 @@ __device__ __forceinline__ void load_level_tables(const Params &p, LevelTables &
         t.W[l] = p.W[l];
         t.H[l] = p.H[l];
         t.start[l] = p.start[l];
-        t.kst[l] = p.kst[l];
+        t.bst[l] = p.bst[l];
+        t.BX[l] = p.BX[l];
         t.sx[l] = p.sx[l];
         t.sy[l] = p.sy[l];
     }
@@ -536,13 +539,21 @@ __device__ __forceinline__ float reduce_scatter(float (&v)[G], int r, unsigned g
     return v[0];
 }
 
-// A sample's cell key for the cell-sorted grad_value: the cell's top-left
-// corner (y0, x0), y0 in [-1, H-1], x0 in [-1, W-1], numbered row-major on a
-// (H+1) x (W+1) grid after the keys of the levels before it; -1 when none of
-// the cell's corners lies in the map ("zeros" beyond the edge), such a sample
-// adds nothing to grad_value.
-__device__ __forceinline__ int cell_key(const Cell &c, int W, int kst) {
-    return c.valid ? kst + (c.y0 + 1) * (W + 1) + (c.x0 + 1) : -1;
+// Tiles of the tile-sorted grad_value.  A sample's cell (top-left corner
+// (y0, x0), y0 in [-1, H-1], x0 in [-1, W-1]) has extended coordinates
+// (ey, ex) = (y0 + 1, x0 + 1) on an (H+1) x (W+1) grid, cut into tiles of
+// kTileCells x kTileCells cells numbered row-major per level after the tiles
+// of the levels before it.  bucket_of returns the tile (within the (b, h))
+// and, in *cell, the cell's index inside it; -1 when none of the cell's
+// corners lies in the map ("zeros" beyond the edge): such a sample adds
+// nothing to grad_value.
+constexpr int kTileCells = 16;
+__device__ __forceinline__ int bucket_of(const Cell &c, int bst, int BX, int *cell) {
+    if (!c.valid) return -1;
+    const int ey = c.y0 + 1, ex = c.x0 + 1;
+    const int ty = ey / kTileCells, tx = ex / kTileCells;
+    *cell = (ey - ty * kTileCells) * kTileCells + (ex - tx * kTileCells);
+    return bst + ty * BX + tx;
 }
 
 // The backward reuses the forward's work split: a group of G lanes per row,
@@ -555,22 +566,18 @@ __device__ __forceinline__ int cell_key(const Cell &c, int W, int kst) {
 //   <g, S>     = sum_i w_i d_i        -> grad_attention_weights
 //   <g, dS/dx> = sum_i dw_i/dx d_i     -> grad_sampling_locations.x = A sx <g, dS/dx>
 //   <g, dS/dy> = sum_i dw_i/dy d_i     -> grad_sampling_locations.y = A sy <g, dS/dy>
-// (corners outside the map read 0: their d_i count as 0).  grad_value
-// receives A w_i g at corner i:
-//   SORT = false: straight into the binary32 accumulator, one
-//                 red.global.add.v4.f32 per lane and corner;
-//   SORT = true : not here.  The owner lane appends its sample to its cell's
-//                 list (entry = row, A, fx, fy, at a slot taken from the
-//                 cell's cursor); msda_gv_reduce_kernel adds the lists up.
+// (corners outside the map read 0: their d_i count as 0).  grad_value, when
+// requested here, receives A w_i g at corner i straight into the binary32
+// accumulator, one red.global.add.v4.f32 per lane and corner (the
+// tile-sorted grad_value runs this kernel without kGradValue).
 // FL: kGradValue|kGradLoc|kGradAttn or kGradValue (exactly these outputs),
 // kGradLoc|kGradAttn (no grad_value; the two others as p.flags says), or -1
 // (everything from p.flags at run time).  PAD as in the forward.
-template <typename T, int VEC, int G, int NCH, int PAD, int FL, bool SORT>
+template <typename T, int VEC, int G, int NCH, int PAD, int FL>
 __global__ void __launch_bounds__(kThreads, row_min_blocks(NCH *VEC, false))
 msda_backward_kernel(const __grid_constant__ Params p, const T *__restrict__ grad_out, const T *__restrict__ value,
                      const float *__restrict__ loc, const float *__restrict__ attn, float *__restrict__ gv_acc,
-                     float *__restrict__ grad_loc, float *__restrict__ grad_attn, int *__restrict__ cursor,
-                     uint4 *__restrict__ entries) {
+                     float *__restrict__ grad_loc, float *__restrict__ grad_attn) {
     __shared__ LevelTables lt;
     __shared__ int4 rec_o[kThreads];
     __shared__ float4 rec_w[kThreads];
@@ -581,7 +588,7 @@ msda_backward_kernel(const __grid_constant__ Params p, const T *__restrict__ gra
     const bool need_v = want_gl || want_ga;  // value is read only for these two
     // attention is read only for these two, and for the logits' gradient
     const bool need_a = want_gv || want_gl || (p.logits && want_ga);
-    const bool scatter = want_gv && !SORT;   // consumers add into grad_value
+    const bool scatter = want_gv;            // consumers add into grad_value
     const int lane = threadIdx.x & 31;
     const int r = lane & (G - 1);
     const int grp = lane / G;
@@ -642,19 +649,6 @@ msda_backward_kernel(const __grid_constant__ Params p, const T *__restrict__ gra
                 if (live) cr = corners_of(c, A, W, H, lt.start[l], sP);
                 wo[mypos] = make_int4(cr.o[0], cr.o[1], cr.o[2], cr.o[3]);
                 ww[mypos] = make_float4(cr.w[0], cr.w[1], cr.w[2], cr.w[3]);
-                if constexpr (SORT) {
-                    if (want_gv && live) {
-                        const int key = cell_key(c, W, lt.kst[l]);
-                        if (key >= 0) {
-                            const uint32_t gkey =
-                                (rw.b * (uint32_t)p.N_h + rw.h) * (uint32_t)p.K_bh + (uint32_t)key;
-                            const uint32_t slot = (uint32_t)atomicAdd(cursor + gkey, 1);
-                            if (slot < p.capacity)
-                                entries[slot] = make_uint4(rw.bqh, __float_as_uint(A), __float_as_uint(c.fx),
-                                                           __float_as_uint(c.fy));
-                        }
-                    }
-                }
             }
             __syncwarp(gmask);
             // consume phase: the group's samples in order
@@ -750,115 +744,236 @@ msda_backward_kernel(const __grid_constant__ Params p, const T *__restrict__ gra
     }
 }
 
-// ---------------------------------------------------------------- cell-sorted grad_value
+// ---------------------------------------------------------------- tile-sorted grad_value
 // grad_value[pixel] = sum over samples s and corners i of s's cell at that
 // pixel of A_s w_i(s) g_{row(s)}.  Scattered one corner at a time this is four
-// C_h-wide atomic adds per sample, and L2's reduction throughput bounds the
-// backward.  Instead the samples are grouped by cell (counting sort on the
-// cell key), and one group of lanes per cell sums its samples' rows of
-// grad_output, weighted for each of the cell's four corners, in registers:
-// one row load per sample, and four atomic adds per cell instead of per
-// sample.
-//   1. msda_count_kernel     counts[key] = samples whose cell is key
-//   2. msda_scan_*_kernel    offsets = exclusive prefix sum of counts;
-//                            cursor = offsets
-//   3. msda_backward_kernel<SORT = true> appends each sample at
-//                            entries[atomicAdd(cursor[key], 1)]
-//   4. msda_gv_reduce_kernel adds the lists into the accumulator
-// Key order within a list is the order of the atomics, so grad_value's
-// summation order (not its value) varies from call to call, as with direct
-// atomics.
+// C_h-wide binary32 reduction lines per sample, and the GPU's reduction rate
+// (about 6.7 TB/s of payload, one 128-byte line per ~6 SM cycles) bounds the
+// backward.  The tile-sorted path first groups the samples by cell and sums
+// each cell's samples in registers, so a cell costs four reduction lines per
+// run of its samples instead of four per sample:
+//   1. msda_tile_count_kernel   counts[tile][part]: samples of partition block
+//                               `part` (a run of rows) in tile `tile`
+//                               (kTileCells^2 cells of one level and (b, h)),
+//                               counted in shared memory: no global atomics
+//   2. scan                     offsets = exclusive prefix sum of the counts in
+//                               (tile, part) order: a tile's samples become one
+//                               contiguous range, split by partition block
+//   3. msda_tile_items_kernel   chunks[tile] = ceil(samples of tile / kChunk),
+//      scan                     then chunk offsets
+//   4. msda_tile_append_kernel  each partition block writes its samples'
+//                               entries (row | cell << 24, A, fx, fy) into its
+//                               own slots of each tile (shared cursors)
+//   5. msda_tile_reduce_kernel  one block per chunk of a tile: counting sort of
+//                               the chunk's entries by cell in shared memory;
+//                               each group of G lanes sweeps an equal share of
+//                               the sorted entries with several grad_output
+//                               rows in flight, sums each cell's samples times
+//                               its four corner weights in registers and adds
+//                               them to the accumulator when the cell changes
+//                               (red.global.add.v4.f32).
+// It is used for calls whose only output is grad_value: next to the other two
+// gradients, the fused row kernel overlaps the direct atomics with the value
+// gather and is faster.
+// Within a (tile, part) segment entries are in shared-atomic order, so
+// grad_value's summation order (not its value) varies from call to call.
+constexpr int kChunk = 4096;         // entries of one reduction block
+constexpr int kEntryCellShift = 24;  // entry.x = row | cell << 24 (rows < 2^24, cells < 2^8)
+static_assert(kTileCells * kTileCells <= (1 << (32 - kEntryCellShift)), "cell index must fit above the row");
 
-// Four consecutive samples per thread, in memory order (b, q, h, l, p): the
-// loads of all four are issued before any key is formed, so each thread has
-// several loads in flight.
+// Exclusive prefix sum of n int32 counts, in tiles of kScanTile: pass 1 sums
+// each tile, pass 2 scans each tile after the sums of the tiles before it, in
+// place (counts become offsets), and writes the grand total to offsets[n].
+constexpr int kScanThreads = 1024;
+constexpr int kScanPer = 4;
+constexpr int kScanTile = kScanThreads * kScanPer;
+__global__ void msda_scan_tiles_kernel(const int *__restrict__ counts, uint32_t n, int *__restrict__ tile_sums);
+__global__ void msda_scan_apply_kernel(int *__restrict__ offsets, uint32_t n, const int *__restrict__ tile_sums);
+
+// The tile of one sample of row `row` (rows in (b, h, q) order), its cell in
+// the tile, and the sample's cell fractions; -1 when it adds nothing.
+template <int PAD>
+__device__ __forceinline__ int tile_of_sample(const Params &p, const LevelTables &lt, const float *loc, uint32_t row,
+                                              int j, int *cell, Cell *cout, uint32_t *bh_out, uint32_t *bqh_out) {
+    const Row rw = decode_row(p, row);
+    const int64_t lo = rw.b * p.l_sB + (int64_t)((rw.q * (uint32_t)p.N_h + rw.h) * (uint32_t)p.NLP + j) * p.l_sJ;
+    const int l = (int)p.div_p.div((uint32_t)j);
+    const int W = lt.W[l], H = lt.H[l];
+    const Cell c = make_cell<PAD>(ldl(loc, lo, p.loc_dt), ldl(loc, lo + p.l_sXY, p.loc_dt), lt.sx[l], lt.sy[l], p.off,
+                                  W, H, p.padding);
+    *cout = c;
+    *bh_out = rw.b * (uint32_t)p.N_h + rw.h;
+    *bqh_out = rw.bqh;
+    return bucket_of(c, lt.bst[l], lt.BX[l], cell);
+}
+
+// Partition block `part` owns rows [part * part_rows, +part_rows) of the
+// (b, h, q) order; their samples fall in the tiles of at most p.span (b, h)
+// pairs, the first being (first row) / N_q.  Shared memory: p.span * p.NB ints.
 template <int PAD>
 __global__ void __launch_bounds__(256)
-msda_count_kernel(const __grid_constant__ Params p, const float *__restrict__ loc, int *__restrict__ counts) {
+msda_tile_count_kernel(const __grid_constant__ Params p, const float *__restrict__ loc, int *__restrict__ counts) {
+    extern __shared__ int hist[];
     __shared__ LevelTables lt;
     load_level_tables(p, lt);
-    constexpr int U = 4;
-    const uint32_t total = p.rows * (uint32_t)p.NLP;
-    const uint32_t per_batch = (uint32_t)p.N_q * (uint32_t)p.N_h * (uint32_t)p.NLP;
-    const uint32_t stride = gridDim.x * blockDim.x * U;
-    for (uint32_t s0 = (blockIdx.x * blockDim.x + threadIdx.x) * U; s0 < total; s0 += stride) {
-        float u[U], v[U];
-        uint32_t b[U];
-#pragma unroll
-        for (int t = 0; t < U; ++t) {
-            const uint32_t s = s0 + t;
-            u[t] = v[t] = 0.0f;
-            b[t] = 0;
-            if (s < total) {
-                b[t] = s / per_batch;
-                const int64_t lo = b[t] * p.l_sB + (int64_t)(s - b[t] * per_batch) * p.l_sJ;
-                u[t] = ldl(loc, lo, p.loc_dt);
-                v[t] = ldl(loc, lo + p.l_sXY, p.loc_dt);
+    const uint32_t part = blockIdx.x;
+    const uint32_t r0 = part * p.part_rows;
+    const uint32_t r1 = min(p.rows, r0 + p.part_rows);
+    if (r0 >= r1) return;  // uniform over the block
+    const uint32_t bh0 = p.div_q.div(r0);
+    for (int i = threadIdx.x; i < p.span * p.NB; i += blockDim.x) hist[i] = 0;
+    __syncthreads();
+    const uint32_t n = (r1 - r0) * (uint32_t)p.NLP;
+    for (uint32_t t = threadIdx.x; t < n; t += blockDim.x) {
+        const uint32_t row = r0 + p.div_nlp.div(t);
+        const int j = (int)(t - (row - r0) * (uint32_t)p.NLP);
+        int cell;
+        Cell c;
+        uint32_t bh, bqh;
+        const int tile = tile_of_sample<PAD>(p, lt, loc, row, j, &cell, &c, &bh, &bqh);
+        if (tile >= 0) atomicAdd(hist + (int)(bh - bh0) * p.NB + tile, 1);
+    }
+    __syncthreads();
+    // every (tile, part) count of this block's (b, h) range, zeros included
+    const int here = (int)(p.div_q.div(r1 - 1) - bh0 + 1) * p.NB;
+    for (int i = threadIdx.x; i < here; i += blockDim.x)
+        counts[(size_t)(bh0 * (uint32_t)p.NB + (uint32_t)i) * p.parts + part] = hist[i];
+}
+
+// chunks[tile] = ceil(samples of tile / kChunk); offsets are in (tile, part) order.
+__global__ void msda_tile_items_kernel(const __grid_constant__ Params p, const int *__restrict__ offsets,
+                                       int *__restrict__ chunks);
+
+template <int PAD>
+__global__ void __launch_bounds__(256)
+msda_tile_append_kernel(const __grid_constant__ Params p, const float *__restrict__ loc,
+                        const float *__restrict__ attn, const int *__restrict__ offsets,
+                        uint4 *__restrict__ entries) {
+    extern __shared__ int cur[];  // p.span * p.NB
+    __shared__ LevelTables lt;
+    load_level_tables(p, lt);
+    const uint32_t part = blockIdx.x;
+    const uint32_t r0 = part * p.part_rows;
+    const uint32_t r1 = min(p.rows, r0 + p.part_rows);
+    if (r0 >= r1) return;
+    const uint32_t bh0 = p.div_q.div(r0);
+    const int here = (int)(p.div_q.div(r1 - 1) - bh0 + 1) * p.NB;
+    for (int i = threadIdx.x; i < here; i += blockDim.x)
+        cur[i] = offsets[(size_t)(bh0 * (uint32_t)p.NB + (uint32_t)i) * p.parts + part];
+    __syncthreads();
+    const uint32_t n = (r1 - r0) * (uint32_t)p.NLP;
+    for (uint32_t t = threadIdx.x; t < n; t += blockDim.x) {
+        const uint32_t row = r0 + p.div_nlp.div(t);
+        const int j = (int)(t - (row - r0) * (uint32_t)p.NLP);
+        int cell;
+        Cell c;
+        uint32_t bh, bqh;
+        const int tile = tile_of_sample<PAD>(p, lt, loc, row, j, &cell, &c, &bh, &bqh);
+        if (tile >= 0) {
+            float A = ldl(attn, (int64_t)bqh * p.NLP + j, p.loc_dt);
+            if (p.logits) {  // softmax over the row's logits (recomputed per sample: rows are short)
+                float m = -INFINITY, sum = 0.0f;
+                for (int k = 0; k < p.NLP; ++k) m = fmaxf(m, ldl(attn, (int64_t)bqh * p.NLP + k, p.loc_dt));
+                for (int k = 0; k < p.NLP; ++k) sum += expf(ldl(attn, (int64_t)bqh * p.NLP + k, p.loc_dt) - m);
+                A = expf(A - m) * (1.0f / sum);
             }
-        }
-#pragma unroll
-        for (int t = 0; t < U; ++t) {
-            const uint32_t s = s0 + t;
-            if (s < total) {
-                const uint32_t rowq = p.div_nlp.div(s);  // (b * N_q + q) * N_h + h
-                const uint32_t j = s - rowq * (uint32_t)p.NLP;
-                const uint32_t h = rowq - p.div_h.div(rowq) * (uint32_t)p.N_h;
-                const int l = (int)p.div_p.div(j);
-                const int W = lt.W[l], H = lt.H[l];
-                const Cell c = make_cell<PAD>(u[t], v[t], lt.sx[l], lt.sy[l], p.off, W, H, p.padding);
-                const int key = cell_key(c, W, lt.kst[l]);
-                if (key >= 0)
-                    atomicAdd(counts + (b[t] * (uint32_t)p.N_h + h) * (uint32_t)p.K_bh + (uint32_t)key, 1);
-            }
+            const uint32_t slot = (uint32_t)atomicAdd(cur + (int)(bh - bh0) * p.NB + tile, 1);
+            if (slot < p.capacity)
+                entries[slot] = make_uint4(bqh | ((uint32_t)cell << kEntryCellShift), __float_as_uint(A),
+                                           __float_as_uint(c.fx), __float_as_uint(c.fy));
         }
     }
 }
 
-// Exclusive prefix sum of n counts, in tiles of kScanTile: pass 1 sums each
-// tile, pass 2 scans each tile after the sums of the tiles before it, in
-// place (counts become offsets), copies the offsets to cursor and writes the
-// grand total to offsets[n].
-constexpr int kScanThreads = 1024;
-constexpr int kScanPer = 4;
-constexpr int kScanTile = kScanThreads * kScanPer;
+// Shared memory of msda_tile_reduce_kernel: the chunk's entries and their order.
+constexpr size_t kTileReduceSmem = (size_t)kChunk * sizeof(uint4) + (size_t)kChunk * sizeof(uint16_t);
 
-__global__ void msda_scan_tiles_kernel(const int *__restrict__ counts, uint32_t n, int *__restrict__ tile_sums);
-__global__ void msda_scan_apply_kernel(int *__restrict__ offsets, uint32_t n, const int *__restrict__ tile_sums,
-                                       int *__restrict__ cursor);
-
-// One group of G lanes per cell key, keys taken level by level in the order
-// p.ilev (levels with the fewest pixels, hence the longest lists, first).  The
-// group walks the key's list: every lane loads the entry (row, A, fx, fy),
-// forms the four corner weights A(1-fx)(1-fy), A fx(1-fy), A(1-fx)fy, A fx fy
-// and adds weight * (its chunks of grad_output's row) into four per-corner
-// sums; then it adds each sum whose corner lies in the map into the
-// accumulator (red.global.add.v4.f32).
 template <typename T, int VEC, int G, int NCH>
 __global__ void __launch_bounds__(256, 3)
-msda_gv_reduce_kernel(const __grid_constant__ Params p, const T *__restrict__ grad_out,
-                      const int *__restrict__ offsets, const uint4 *__restrict__ entries,
-                      float *__restrict__ gv_acc) {
+msda_tile_reduce_kernel(const __grid_constant__ Params p, const T *__restrict__ grad_out,
+                        const int *__restrict__ offsets, const int *__restrict__ chunk_start,
+                        const uint4 *__restrict__ entries, float *__restrict__ gv_acc) {
     constexpr int GPB = 256 / G;
+    constexpr int NCELL = kTileCells * kTileCells;
+    extern __shared__ __align__(16) unsigned char smem[];
+    uint4 *ent = reinterpret_cast<uint4 *>(smem);
+    uint16_t *order = reinterpret_cast<uint16_t *>(ent + kChunk);
+    __shared__ int ccount[NCELL];
+    __shared__ int s_tile, s_k;
+
+    const int total_items = chunk_start[p.nbins];
+    if ((int)blockIdx.x >= total_items) return;  // uniform over the block
+    if (threadIdx.x == 0) {  // the tile whose chunks include this block: last tile with chunk_start <= item
+        uint32_t lo = 0, hi = p.nbins;  // chunk_start[lo] <= item < chunk_start[hi]
+        while (hi - lo > 1) {
+            const uint32_t mid = (lo + hi) / 2;
+            if (chunk_start[mid] <= (int)blockIdx.x) lo = mid;
+            else hi = mid;
+        }
+        s_tile = (int)lo;
+        s_k = (int)blockIdx.x - chunk_start[lo];
+    }
+    for (int i = threadIdx.x; i < NCELL; i += blockDim.x) ccount[i] = 0;
+    __syncthreads();
+    const uint32_t tile = (uint32_t)s_tile;
+    const int e0 = offsets[(size_t)tile * p.parts] + s_k * kChunk;
+    const int ne = min(offsets[(size_t)(tile + 1) * p.parts], e0 + kChunk) - e0;
+    // the tile's (b, h), level and position
+    const uint32_t bh = tile / (uint32_t)p.NB;
+    const int lb = (int)(tile - bh * (uint32_t)p.NB);
+    int l = 0;
+    while (l + 1 < p.N_l && p.bst[l + 1] <= lb) ++l;
+    const int rel = lb - p.bst[l];
+    const int ty = rel / p.BX[l], tx = rel - ty * p.BX[l];
+    const int W = p.W[l], H = p.H[l];
+    const int y_org = ty * kTileCells - 1, x_org = tx * kTileCells - 1;  // pixel of cell (0,0)'s top-left corner
+
+    // counting sort of the chunk's entries by cell
+    for (int i = threadIdx.x; i < ne; i += blockDim.x) {
+        const uint4 e = __ldg(entries + e0 + i);
+        ent[i] = e;
+        atomicAdd(ccount + (int)(e.x >> kEntryCellShift), 1);
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) {  // exclusive scan of the NCELL counts, NCELL/32 per lane
+        int v[NCELL / 32], sum = 0;
+#pragma unroll
+        for (int i = 0; i < NCELL / 32; ++i) {
+            v[i] = ccount[threadIdx.x * (NCELL / 32) + i];
+            sum += v[i];
+        }
+        int incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if ((int)threadIdx.x >= o) incl += y;
+        }
+        int run = incl - sum;
+#pragma unroll
+        for (int i = 0; i < NCELL / 32; ++i) {
+            ccount[threadIdx.x * (NCELL / 32) + i] = run;  // becomes the cell's cursor
+            run += v[i];
+        }
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < ne; i += blockDim.x)
+        order[atomicAdd(ccount + (int)(ent[i].x >> kEntryCellShift), 1)] = (uint16_t)i;
+    __syncthreads();
+
     const int lane = threadIdx.x & 31;
     const int r = lane & (G - 1);
-    const uint32_t item = blockIdx.x * GPB + threadIdx.x / G;
-    if (item >= p.nkeys) return;  // the whole group leaves together
-    int pos = 0;
-    while (item >= p.iend[pos]) ++pos;
-    const int l = p.ilev[pos];
-    const uint32_t rel = item - (pos ? p.iend[pos - 1] : 0u);
-    const int W = p.W[l], H = p.H[l];
-    const uint32_t KL = (uint32_t)(H + 1) * (uint32_t)(W + 1);
-    const uint32_t bh = rel / KL;
-    const int cl = (int)(rel - bh * KL);
-    const int y0 = cl / (W + 1) - 1, x0 = cl % (W + 1) - 1;
-    const uint32_t gkey = bh * (uint32_t)p.K_bh + (uint32_t)p.kst[l] + (uint32_t)cl;
-    const int beg = offsets[gkey], end = offsets[gkey + 1];
-    if (beg >= end) return;
+    const int grp = threadIdx.x / G;
     int nk = 0;
 #pragma unroll
     for (int k = 0; k < NCH; ++k) nk += (k * G + r < p.chunks);
-
+    const T *gbase = grad_out + r * VEC;
+    const uint32_t b = p.div_h.div(bh), h = bh - b * (uint32_t)p.N_h;
+    float *gb = gv_acc + b * p.v_sB + (int64_t)h * p.v_sH + r * VEC;
+    // Each group sweeps an equal share of the cell-sorted entries with U
+    // grad_output rows in flight, summing the current cell's samples in
+    // registers, and adds the four corner sums to the accumulator when the cell
+    // changes.
+    const int s_beg = (int)(((int64_t)ne * grp) / GPB), s_end = (int)(((int64_t)ne * (grp + 1)) / GPB);
     float acc[4][NCH][VEC];
 #pragma unroll
     for (int i = 0; i < 4; ++i)
@@ -866,47 +981,62 @@ msda_gv_reduce_kernel(const __grid_constant__ Params p, const T *__restrict__ gr
         for (int k = 0; k < NCH; ++k)
 #pragma unroll
             for (int e = 0; e < VEC; ++e) acc[i][k][e] = 0.0f;
-    const T *gbase = grad_out + r * VEC;
-    constexpr int U = 8;  // entries in flight
-    for (int e0 = beg; e0 < end; e0 += U) {
-        uint4 ent[U];
+    int cur_cell = -1;
+    auto flush = [&]() {  // the current cell's four corner sums, corners in the map only
+        if (cur_cell < 0) return;
+        const int cy = cur_cell / kTileCells, cx = cur_cell - cy * kTileCells;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int y = y_org + cy + (i >> 1), x = x_org + cx + (i & 1);
+            if ((unsigned)y < (unsigned)H && (unsigned)x < (unsigned)W) {
+                float *dst = gb + (int64_t)(p.start[l] + y * W + x) * p.v_sP;
+#pragma unroll
+                for (int k = 0; k < NCH; ++k)
+                    if (k < nk) RedIO<VEC>::add(dst + k * G * VEC, acc[i][k], 1.0f);
+            }
+#pragma unroll
+            for (int k = 0; k < NCH; ++k)
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) acc[i][k][e] = 0.0f;
+        }
+    };
+    constexpr int U = 8;  // grad_output rows in flight
+    for (int s0 = s_beg; s0 < s_end; s0 += U) {
+        int ei[U];
         float gv[U][NCH][VEC];
 #pragma unroll
         for (int t = 0; t < U; ++t) {
-            ent[t] = e0 + t < end ? __ldg(entries + e0 + t) : make_uint4(0u, 0u, 0u, 0u);
-            const uint32_t row = ent[t].x < p.rows ? ent[t].x : 0u;  // an entry's row is always < rows
+            ei[t] = s0 + t < s_end ? (int)order[s0 + t] : -1;
+            uint32_t row = ei[t] >= 0 ? (ent[ei[t]].x & ((1u << kEntryCellShift) - 1u)) : 0u;
+            if (row >= p.rows) row = 0;  // an entry's row is always < rows
 #pragma unroll
             for (int k = 0; k < NCH; ++k)
                 if (k < nk) VecIO<T, VEC>::load(gbase + (int64_t)row * p.C_h + k * G * VEC, gv[t][k]);
         }
 #pragma unroll
         for (int t = 0; t < U; ++t) {
-            const float A = __uint_as_float(ent[t].y), fx = __uint_as_float(ent[t].z),
-                        fy = __uint_as_float(ent[t].w);
-            const float A1 = A * fx;
-            const float ax0 = A - A1, ax1 = A1, ay0 = 1.0f - fy, ay1 = fy;
-            const float w[4] = {ay0 * ax0, ay0 * ax1, ay1 * ax0, ay1 * ax1};
+            if (ei[t] >= 0) {
+                const uint4 en = ent[ei[t]];
+                const int cell = (int)(en.x >> kEntryCellShift);
+                if (cell != cur_cell) {
+                    flush();
+                    cur_cell = cell;
+                }
+                const float A = __uint_as_float(en.y), fx = __uint_as_float(en.z), fy = __uint_as_float(en.w);
+                const float A1 = A * fx;
+                const float ax0 = A - A1, ax1 = A1, ay0 = 1.0f - fy, ay1 = fy;
+                const float w[4] = {ay0 * ax0, ay0 * ax1, ay1 * ax0, ay1 * ax1};
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
+                for (int i = 0; i < 4; ++i)
 #pragma unroll
-                for (int k = 0; k < NCH; ++k)
-                    if (k < nk)
+                    for (int k = 0; k < NCH; ++k)
+                        if (k < nk)
 #pragma unroll
-                        for (int e = 0; e < VEC; ++e) acc[i][k][e] = fmaf(w[i], gv[t][k][e], acc[i][k][e]);
+                            for (int e = 0; e < VEC; ++e) acc[i][k][e] = fmaf(w[i], gv[t][k][e], acc[i][k][e]);
+            }
         }
     }
-    const uint32_t b = p.div_h.div(bh), h = bh - b * (uint32_t)p.N_h;
-    float *gb = gv_acc + b * p.v_sB + (int64_t)h * p.v_sH + r * VEC;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int y = y0 + (i >> 1), x = x0 + (i & 1);
-        if ((unsigned)y < (unsigned)H && (unsigned)x < (unsigned)W) {
-            float *dst = gb + (int64_t)(p.start[l] + y * W + x) * p.v_sP;
-#pragma unroll
-            for (int k = 0; k < NCH; ++k)
-                if (k < nk) RedIO<VEC>::add(dst + k * G * VEC, acc[i][k], 1.0f);
-        }
-    }
+    flush();
 }
 
 // ---------------------------------------------------------------- helpers
@@ -929,32 +1059,33 @@ inline cudaError_t launch_forward(const Params &p, bool vec, int G, int NCH, con
 }
 
 // Buffers of the backward: the binary32 grad_value accumulator and, for the
-// cell-sorted grad_value, the key counts / offsets (nkeys + 1), the cursors
-// (nkeys), the tile sums of the scan and the entries (capacity).
+// tile-sorted grad_value, the (tile, part) counts / offsets (nbins * parts + 1),
+// the per-tile chunk counts / offsets (nbins + 1), the scans' tile sums and the
+// entries (capacity).
 struct BwdBuffers {
     float *gv_acc;
     float *grad_loc, *grad_attn;
-    int *offsets, *cursor, *tile_sums;
+    int *offsets, *chunks, *tile_sums;
     uint4 *entries;
 };
 template <typename T, int PAD>
-cudaError_t launch_backward_pad(const Params &p, int G, int NCH, bool sort, const T *grad_out, const T *value,
+cudaError_t launch_backward_pad(const Params &p, int G, int NCH, const T *grad_out, const T *value,
                                 const float *loc, const float *attn, const BwdBuffers &bb, cudaStream_t stream);
 // Dispatch on vector path / padding to the launch_backward_pad instantiations.
 template <typename T>
-inline cudaError_t launch_backward(const Params &p, bool vec, int G, int NCH, bool sort, const T *grad_out,
-                                   const T *value, const float *loc, const float *attn, const BwdBuffers &bb,
-                                   cudaStream_t stream) {
+inline cudaError_t launch_backward(const Params &p, bool vec, int G, int NCH, const T *grad_out, const T *value,
+                                   const float *loc, const float *attn, const BwdBuffers &bb, cudaStream_t stream) {
     if (p.rows == 0) return cudaSuccess;
-    if (!vec) return launch_backward_pad<T, -1>(p, G, NCH, sort, grad_out, value, loc, attn, bb, stream);
-    if (p.padding == 0) return launch_backward_pad<T, 0>(p, G, NCH, sort, grad_out, value, loc, attn, bb, stream);
-    return launch_backward_pad<T, 1>(p, G, NCH, sort, grad_out, value, loc, attn, bb, stream);
+    if (!vec) return launch_backward_pad<T, -1>(p, G, NCH, grad_out, value, loc, attn, bb, stream);
+    if (p.padding == 0) return launch_backward_pad<T, 0>(p, G, NCH, grad_out, value, loc, attn, bb, stream);
+    return launch_backward_pad<T, 1>(p, G, NCH, grad_out, value, loc, attn, bb, stream);
 }
-// Cell-sorted grad_value, steps 1-2 (count, scan) and 4 (reduce).
-cudaError_t launch_sort_keys(const Params &p, const float *loc, const BwdBuffers &bb, cudaStream_t stream);
+// Tile-sorted grad_value, steps 1-4 (count, scans, chunks, append) and 5 (reduce).
+cudaError_t launch_tile_partition(const Params &p, const float *loc, const float *attn, const BwdBuffers &bb,
+                                  cudaStream_t stream);
 template <typename T, bool VECTOR>
-cudaError_t launch_gv_reduce(const Params &p, int G, int NCH, const T *grad_out, const BwdBuffers &bb,
-                             cudaStream_t stream);
+cudaError_t launch_tile_reduce(const Params &p, int G, int NCH, const T *grad_out, const BwdBuffers &bb,
+                               cudaStream_t stream);
 cudaError_t launch_zero_f32(float *p, int64_t n, cudaStream_t stream);
 cudaError_t launch_f32_to_bf16(const float *acc, __nv_bfloat16 *out, int64_t n, cudaStream_t stream);
 

@@ -72,34 +72,29 @@ cudaError_t launch_forward_path(const Params &p, int G, int NCH, const T *value,
     return cudaErrorInvalidConfiguration;
 }
 
-template <typename T, int V, int GG, int NN, int PAD, int FL, bool SORT>
+template <typename T, int V, int GG, int NN, int PAD, int FL>
 cudaError_t bwd_launch(const Params &p, const T *grad_out, const T *value, const float *loc, const float *attn,
                        const BwdBuffers &bb, cudaStream_t stream) {
-    auto kernel = msda_backward_kernel<T, V, GG, NN, PAD, FL, SORT>;
+    auto kernel = msda_backward_kernel<T, V, GG, NN, PAD, FL>;
     const unsigned blocks = row_grid(kernel, GG, p);
-    kernel<<<blocks, kThreads, 0, stream>>>(p, grad_out, value, loc, attn, bb.gv_acc, bb.grad_loc, bb.grad_attn,
-                                            bb.cursor, bb.entries);
+    kernel<<<blocks, kThreads, 0, stream>>>(p, grad_out, value, loc, attn, bb.gv_acc, bb.grad_loc, bb.grad_attn);
     return cudaGetLastError();
 }
 
+// p.flags: the outputs this launch produces (without kGradValue when the
+// tile-sorted grad_value does that part).
 template <typename T, int V, int GG, int NN, int PAD>
-cudaError_t bwd_flags(const Params &p, bool sort, const T *grad_out, const T *value, const float *loc,
-                      const float *attn, const BwdBuffers &bb, cudaStream_t stream) {
+cudaError_t bwd_flags(const Params &p, const T *grad_out, const T *value, const float *loc, const float *attn,
+                      const BwdBuffers &bb, cudaStream_t stream) {
     constexpr int ALL = kGradValue | kGradLoc | kGradAttn;
-#define MSDA_BWD(FL, SO) return bwd_launch<T, V, GG, NN, PAD, FL, SO>(p, grad_out, value, loc, attn, bb, stream)
+#define MSDA_BWD(FL) return bwd_launch<T, V, GG, NN, PAD, FL>(p, grad_out, value, loc, attn, bb, stream)
     if constexpr (PAD < 0 || !specialised_shape(GG, NN)) {
-        if (sort) MSDA_BWD(-1, true);
-        MSDA_BWD(-1, false);
+        MSDA_BWD(-1);
     } else {
-        if (!(p.flags & kGradValue)) MSDA_BWD(kGradLoc | kGradAttn, false);
-        if (sort) {
-            if (p.flags == ALL) MSDA_BWD(ALL, true);
-            if (p.flags == kGradValue) MSDA_BWD(kGradValue, true);
-            MSDA_BWD(-1, true);
-        }
-        if (p.flags == ALL) MSDA_BWD(ALL, false);
-        if (p.flags == kGradValue) MSDA_BWD(kGradValue, false);
-        MSDA_BWD(-1, false);
+        if (!(p.flags & kGradValue)) MSDA_BWD(kGradLoc | kGradAttn);
+        if (p.flags == ALL) MSDA_BWD(ALL);
+        if (p.flags == kGradValue) MSDA_BWD(kGradValue);
+        MSDA_BWD(-1);
     }
 #undef MSDA_BWD
 }
@@ -111,16 +106,16 @@ cudaError_t bwd_flags(const Params &p, bool sort, const T *grad_out, const T *va
 //   PAD -2   : vector path, wide shapes, padding and outputs read at run time;
 //   PAD -1   : scalar path (unaligned pointers or C_h not a multiple of 4).
 template <typename T, int PAD>
-cudaError_t launch_backward_pad(const Params &p, int G, int NCH, bool sort, const T *grad_out, const T *value,
+cudaError_t launch_backward_pad(const Params &p, int G, int NCH, const T *grad_out, const T *value,
                                 const float *loc, const float *attn, const BwdBuffers &bb, cudaStream_t stream) {
     constexpr int V = PAD == -1 ? 1 : BwdVecWidth<T>::value;
 #define MSDA_BWD_CASE(GG, NN)                                                                     \
     if constexpr (reachable(GG, NN, MSDA_BWD_LANES)) {                                            \
         if (G == GG && NCH == NN) {                                                               \
             if constexpr (PAD == -1 || (PAD == -2) != specialised_shape(GG, NN))                  \
-                return bwd_flags<T, V, GG, NN, PAD>(p, sort, grad_out, value, loc, attn, bb, stream); \
+                return bwd_flags<T, V, GG, NN, PAD>(p, grad_out, value, loc, attn, bb, stream);   \
             else if constexpr (PAD >= 0)                                                          \
-                return launch_backward_pad<T, -2>(p, G, NCH, sort, grad_out, value, loc, attn, bb, \
+                return launch_backward_pad<T, -2>(p, G, NCH, grad_out, value, loc, attn, bb,      \
                                                   stream);                                        \
             else                                                                                  \
                 return cudaErrorInvalidConfiguration;                                             \
@@ -131,19 +126,23 @@ cudaError_t launch_backward_pad(const Params &p, int G, int NCH, bool sort, cons
     return cudaErrorInvalidConfiguration;
 }
 
-// Cell-sorted grad_value, step 4: one group per key.
+// Tile-sorted grad_value, step 5: one block per chunk of a tile's samples.
 template <typename T, bool VECTOR>
-cudaError_t launch_gv_reduce(const Params &p, int G, int NCH, const T *grad_out, const BwdBuffers &bb,
-                             cudaStream_t stream) {
-    if (p.nkeys == 0) return cudaSuccess;
+cudaError_t launch_tile_reduce(const Params &p, int G, int NCH, const T *grad_out, const BwdBuffers &bb,
+                               cudaStream_t stream) {
+    if (p.nbins == 0) return cudaSuccess;
     constexpr int V = VECTOR ? BwdVecWidth<T>::value : 1;
+    // chunks <= tiles + samples / kChunk (a tile's last chunk may be partial)
+    const uint64_t blocks = (uint64_t)p.nbins + ((uint64_t)p.rows * p.NLP) / kChunk + 1;
 #define MSDA_RED_CASE(GG, NN)                                                                     \
     if constexpr (reachable(GG, NN, MSDA_BWD_LANES)) {                                            \
         if (G == GG && NCH == NN) {                                                               \
-            constexpr unsigned gpb = 256 / GG;                                                    \
-            const unsigned blocks = (unsigned)((p.nkeys + gpb - 1) / gpb);                        \
-            msda_gv_reduce_kernel<T, V, GG, NN><<<blocks, 256, 0, stream>>>(p, grad_out, bb.offsets, \
-                                                                          bb.entries, bb.gv_acc); \
+            auto kernel = msda_tile_reduce_kernel<T, V, GG, NN>;                                  \
+            const cudaError_t e =                                                                 \
+                cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTileReduceSmem); \
+            if (e != cudaSuccess) return e;                                                       \
+            kernel<<<(unsigned)blocks, 256, kTileReduceSmem, stream>>>(p, grad_out, bb.offsets, bb.chunks, \
+                                                                       bb.entries, bb.gv_acc);   \
             return cudaGetLastError();                                                            \
         }                                                                                         \
     }
