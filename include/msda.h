@@ -139,11 +139,13 @@ int msda_forward(const msda_desc *desc, const void *value, const void *sampling_
  *   - B*L*N_h*C_h*4, a binary32 grad_value accumulator, when value_dtype is
  *     BF16;
  *   - when the problem has at least two samples per bilinear cell on average
- *     (S = B*N_q*N_h*N_l*N_p >= 2*K with K = B*N_h*sum_l (H_l+1)*(W_l+1) cell
- *     keys, and S < 2^31): (2K+1)*4 bytes of cell counts and cursors, 4 bytes
- *     per 4096 keys of scan partials and 16*S bytes of per-cell sample
- *     lists, used to sum grad_value per cell when grad_value is the only
- *     requested output.
+ *     (S = B*N_q*N_h*N_l*N_p >= 2*B*N_h*sum_l (H_l+1)*(W_l+1), C_h a multiple
+ *     of 4, S < 2^31 and B*N_h*N_q < 2^24): the buffers of the tile-sorted
+ *     grad_value, which calls with grad_value as the only output use --
+ *     4*(T*P + 1) bytes of per-tile and per-block counts (T tiles of 16x16
+ *     cells over all levels and (b, h), P = min(1024, ceil(B*N_h*N_q/512))
+ *     partition blocks), 4*(T + 1) bytes of chunk counts, the scans' partial
+ *     sums and 16*S bytes of sample entries.
  * The size depends on the descriptor and the flag only.  Returns 0 for an
  * invalid descriptor. */
 size_t msda_backward_workspace_size(const msda_desc *desc, int compute_grad_value);

@@ -85,7 +85,7 @@ extern "C" int msda_backward_noalloc(const msda_desc *desc, const void *grad_out
         if (elems * sizeof(float) > kScratchBytes) return MSDA_ERR_WORKSPACE;
     }
     // grad_value goes straight into the accumulator with atomics here: the
-    // cell-sorted path's buffers grow with the number of samples.
+    // tile-sorted path's buffers grow with the number of samples.
     const size_t need = msda::backward_workspace_bytes(desc, compute_grad_value, false);
     if (need > kScratchBytes) return MSDA_ERR_WORKSPACE;
     void *ws = nullptr;
