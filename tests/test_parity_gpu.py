@@ -98,6 +98,15 @@ def test_channel_counts_sorted(dtype, C_h):
     check_workload(w, flag_sets=[(True, False, False)], check_forward=False)
 
 
+@pytest.mark.parametrize("pad,align", [("zeros", False), ("border", True)])
+def test_sorted_many_levels(pad, align):
+    """The tile-sorted grad_value on 16 levels including 1-pixel rows and
+    columns (tile tables, level boundaries, border clamps)."""
+    levels = tuple((3 + i, 1 + (i * 5) % 7) for i in range(15)) + ((1, 1),)
+    w = _dense(_small("f32", "BNLC", "B2QHLP", align, pad, levels=levels, N_q=100, N_p=2, seed=62))
+    check_workload(w, flag_sets=[(True, False, False)], check_forward=False)
+
+
 @pytest.mark.parametrize("loc_dtype", ["bf16", "f16"])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("N_q,ll", [(37, "BQHLP2"), (150, "B2QHLP")])  # 150: cell-sorted grad_value too
