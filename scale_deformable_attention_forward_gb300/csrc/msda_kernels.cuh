@@ -888,8 +888,11 @@ msda_tile_append_kernel(const __grid_constant__ Params p, const float *__restric
 // Shared memory of msda_tile_reduce_kernel: the chunk's entries and their order.
 constexpr size_t kTileReduceSmem = (size_t)kChunk * sizeof(uint4) + (size_t)kChunk * sizeof(uint16_t);
 
+// 3 blocks per SM (the shared memory allows no more) for one channel chunk a
+// lane; fewer for wider rows, whose 4 x NCH x VEC accumulators a lane need the
+// registers.
 template <typename T, int VEC, int G, int NCH>
-__global__ void __launch_bounds__(256, 3)
+__global__ void __launch_bounds__(256, NCH >= 4 ? 1 : NCH == 2 ? 2 : 3)
 msda_tile_reduce_kernel(const __grid_constant__ Params p, const T *__restrict__ grad_out,
                         const int *__restrict__ offsets, const int *__restrict__ chunk_start,
                         const uint4 *__restrict__ entries, float *__restrict__ gv_acc) {
@@ -1000,7 +1003,7 @@ msda_tile_reduce_kernel(const __grid_constant__ Params p, const T *__restrict__ 
                 for (int e = 0; e < VEC; ++e) acc[i][k][e] = 0.0f;
         }
     };
-    constexpr int U = 8;  // grad_output rows in flight
+    constexpr int U = NCH >= 8 ? 1 : 8 / NCH;  // grad_output rows in flight (32 registers of them)
     for (int s0 = s_beg; s0 < s_end; s0 += U) {
         int ei[U];
         float gv[U][NCH][VEC];

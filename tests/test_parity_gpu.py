@@ -95,7 +95,10 @@ def test_option_matrix_sorted(dtype, vl, ll, align, pad):
 @pytest.mark.parametrize("C_h", [1, 3, 4, 5, 8, 12, 40, 96, 256])
 def test_channel_counts_sorted(dtype, C_h):
     w = _dense(_small(dtype, "BLNC", "BQHLP2", False, "zeros", C_h=C_h, N_q=120, N_h=2, N_p=2, seed=C_h + 100))
-    check_workload(w, flag_sets=[(True, False, False)], check_forward=False)
+    # grad_value alone takes the tile-sorted path; with the other gradients
+    # the direct row kernel runs on the same dense problem
+    check_workload(w, flag_sets=[(True, False, False), (True, True, True), (True, True, False), (True, False, True)],
+                   check_forward=False)
 
 
 @pytest.mark.parametrize("pad,align", [("zeros", False), ("border", True)])
@@ -104,7 +107,7 @@ def test_sorted_many_levels(pad, align):
     columns (tile tables, level boundaries, border clamps)."""
     levels = tuple((3 + i, 1 + (i * 5) % 7) for i in range(15)) + ((1, 1),)
     w = _dense(_small("f32", "BNLC", "B2QHLP", align, pad, levels=levels, N_q=100, N_p=2, seed=62))
-    check_workload(w, flag_sets=[(True, False, False)], check_forward=False)
+    check_workload(w, flag_sets=[(True, False, False), (True, True, True)], check_forward=False)
 
 
 @pytest.mark.parametrize("loc_dtype", ["bf16", "f16"])
@@ -131,8 +134,9 @@ def test_many_levels():
 
 # ------------------------------------------------------------------ flags and untouched outputs
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-def test_disabled_outputs_untouched(dtype):
-    w = _small(dtype, "BLNC", "BQHLP2", False, "zeros", seed=71)
+@pytest.mark.parametrize("N_q", [37, 150])  # 150: grad_value-only calls take the tile-sorted path
+def test_disabled_outputs_untouched(dtype, N_q):
+    w = _small(dtype, "BLNC", "BQHLP2", False, "zeros", N_q=N_q, seed=71)
     d = gen.generate(w)
     t = to_device(d, w.dtype)
     for flags in ALL_FLAGS:
@@ -280,3 +284,24 @@ def test_repeatable():
     assert torch.equal(o1, o2)
     assert torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])
     assert_close(np64(a[0]), np64(b[0]), 1e-5, "grad_value run to run")
+
+
+@pytest.mark.parametrize("pad", ["zeros", "border"])
+def test_repeatable_sorted(pad):
+    """On a problem dense enough for the tile-sorted grad_value: the location
+    and attention gradients are bit-identical from run to run, and grad_value
+    (summed by cell runs in an order that changes from run to run) stays
+    within tolerance, whether it comes alone or with the other two."""
+    w = _dense(_small("f32", "BLNC", "BQHLP2", False, pad, N_q=150, seed=17))
+    d = gen.generate(w)
+    t = to_device(d, w.dtype)
+    runs = []
+    for _ in range(3):
+        runs.append([x.clone() for x in gpu_backward(w, t, d)])
+    gvs = [gpu_backward(w, t, d, (True, False, False))[0].clone() for _ in range(3)]
+    torch.cuda.synchronize()
+    for a in runs[1:]:
+        assert torch.equal(a[1], runs[0][1]) and torch.equal(a[2], runs[0][2])
+        assert_close(np64(a[0]), np64(runs[0][0]), 1e-5, "grad_value run to run")
+    for g in gvs:
+        assert_close(np64(g), np64(runs[0][0]), 1e-5, "tile-sorted grad_value run to run")
