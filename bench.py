@@ -358,6 +358,32 @@ def run_ours(args, w: gen.Workload):
     step_ms = max_over_ranks(step_ms_local, world, dev)
     value = w.samples * world / (step_ms * 1e-3) / 1e9
 
+    # The staged-level forward (msda_forward_staged) under the same protocol,
+    # outside the step: the same output as msda_forward, a different gather.
+    out_st = torch.empty_like(out)
+
+    def fwd_staged():
+        msda.msda_forward_staged(t["value"], data["spatial_shapes"], data["level_start_index"],
+                                 t["sampling_locations"], t["attention_weights"], out=out_st, **kw)
+
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        fwd_staged()
+    ev_st = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    for i in range(K):
+        flush.fill_(float(i))
+        ev_st[i][0].record(stream)
+        fwd_staged()
+        ev_st[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    staged_ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in ev_st), world, dev)
+    staged_same = bool(torch.equal(out_st, out))
+    desc = msda.make_desc((w.B, w.n_queries, w.N_h, w.C_h, w.N_l, w.N_p, w.L), data["spatial_shapes"],
+                          data["level_start_index"], w.value_layout, w.loc_layout, w.align_corners,
+                          w.padding_mode, msda.DTYPE_BF16 if w.dtype == "bf16" else msda.DTYPE_F32)
+    staged_first = msda.staged_levels(desc)
+    staged_timeouts = msda.staged_timeouts()
+
     # End to end: pinned host inputs -> device, forward, backward, results ->
     # pinned host, every step.  Two buffer sets and three streams pipeline the
     # steps the way a production loop would: the inputs of step i+1 are copied
@@ -473,6 +499,12 @@ def run_ours(args, w: gen.Workload):
             "peak": REDUCTION_GBS, "unit": "GB/s",
             "frac": round(w.samples * 4 * w.C_h * 4 / (bwd_mean * 1e-3) / 1e9 / REDUCTION_GBS, 4),
             "peak_source": "red.global.add.v4.f32 microbenchmark on GB300 (random 128-byte lines)"},
+        "forward_staged": {
+            "what": "msda_forward_staged: coarse levels copied to shared memory by TMA, gathered from there",
+            "fwd_ms": round(staged_ms, 6), "direct_fwd_ms": round(fwd_mean, 6),
+            "speedup_vs_direct": round(fwd_mean / staged_ms, 4) if staged_ms > 0 else None,
+            "staged_levels": list(range(staged_first, w.N_l)), "bit_identical_to_direct": staged_same,
+            "timeouts": staged_timeouts},
         "roofline_step": {
             "what": "forward + backward compulsory bytes / step time",
             "achieved": round((fwd_b + bwd_b) / (step_ms * 1e-3) / 1e9, 1), "peak": peak, "unit": "GB/s",

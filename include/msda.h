@@ -133,6 +133,36 @@ typedef struct msda_desc {
 int msda_forward(const msda_desc *desc, const void *value, const void *sampling_locations,
                  const void *attention_weights, void *out, cudaStream_t stream);
 
+/* The forward with a staged gather (the same operation as msda_forward:
+ * "MS Deformable Attention Kernel API Reference", Parameters and Returns;
+ * the page's gather_method chooses how the kernel fetches value rows, and
+ * this is the GPU counterpart of choosing).  Each thread block serves a run of
+ * queries of one (b, h) and first copies the coarsest levels of that head
+ * whose pixels fit 40 KB of shared memory, as TMA tensor copies, into shared
+ * memory; samples on those levels read their corners from there, samples on
+ * finer levels from global memory.  out is bit-identical to msda_forward's.
+ * Arguments, layouts, ownership and errors are msda_forward's.  The staged
+ * kernel applies to binary32 locations and weights, C_h * sizeof(value
+ * element) a multiple of 16 bytes, C_h <= 64, value 16-byte aligned and
+ * L >= 32; otherwise, and when no level
+ * fits, the call runs msda_forward's kernel.  A block whose copy has not
+ * completed after a bounded wait gathers every level from global memory and
+ * is counted (msda_staged_timeouts). */
+int msda_forward_staged(const msda_desc *desc, const void *value, const void *sampling_locations,
+                        const void *attention_weights, void *out, cudaStream_t stream);
+
+/* The number of staged-forward blocks, since the library was loaded, that
+ * gave up waiting for their shared-memory copy (expected 0), in *count.
+ * Synchronises with the device.  Returns MSDA_OK, MSDA_ERR_NULL_POINTER or
+ * MSDA_ERR_CUDA. */
+int msda_staged_timeouts(unsigned int *count);
+
+/* The first level msda_forward_staged stages for this descriptor (levels
+ * first_level..N_l-1 go to shared memory), N_l when it would run
+ * msda_forward's kernel; assumes a 16-byte aligned value.  Host only.
+ * Returns MSDA_OK or the descriptor's validation status. */
+int msda_forward_staged_levels(const msda_desc *desc, int *first_level);
+
 /* Bytes of device workspace msda_backward needs, 0 when compute_grad_value is
  * 0.  With compute_grad_value set it is the sum of (each part starting at a
  * 256-byte boundary of the workspace):

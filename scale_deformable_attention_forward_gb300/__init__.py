@@ -85,6 +85,12 @@ def load_library() -> ctypes.CDLL:
             lib.msda_backward_accumulate.restype = I
             lib.msda_forward_logits.argtypes = [D, P, P, P, P, P]
             lib.msda_forward_logits.restype = I
+            lib.msda_forward_staged.argtypes = [D, P, P, P, P, P]
+            lib.msda_forward_staged.restype = I
+            lib.msda_staged_timeouts.argtypes = [ctypes.POINTER(ctypes.c_uint)]
+            lib.msda_staged_timeouts.restype = I
+            lib.msda_forward_staged_levels.argtypes = [D, ctypes.POINTER(ctypes.c_int)]
+            lib.msda_forward_staged_levels.restype = I
             lib.msda_backward_logits.argtypes = [D, P, P, P, P, I, I, I, P, P, P, P, Z, P]
             lib.msda_backward_logits.restype = I
             lib.msda_status_string.argtypes = [I]
@@ -214,7 +220,8 @@ def _stream(device):
 
 def msda_forward(value, spatial_shapes, level_start_index, sampling_locations, attention_weights,
                  value_layout: str = "BLNC", sampling_locations_layout: str = "BQHLP2",
-                 align_corners: bool = False, padding_mode: str = "zeros", out=None, _logits: bool = False):
+                 align_corners: bool = False, padding_mode: str = "zeros", out=None, _logits: bool = False,
+                 _staged: bool = False):
     """Multi-scale deformable attention forward on the GPU.
 
     value (B,L,N_h,C_h) or (B,N_h,L,C_h), float32 or bfloat16;
@@ -244,12 +251,47 @@ def msda_forward(value, spatial_shapes, level_start_index, sampling_locations, a
         _check(out, "out", value.dtype, (B, N_q, N_h * C_h), dev)
     d = make_desc((B, N_q, N_h, C_h, N_l, N_p, L), shapes, starts, value_layout,
                   sampling_locations_layout, align_corners, padding_mode, vdt, ldt)
-    fn, name = (lib.msda_forward_logits, "msda_forward_logits") if _logits else (lib.msda_forward, "msda_forward")
+    fn, name = ((lib.msda_forward_logits, "msda_forward_logits") if _logits else
+                (lib.msda_forward_staged, "msda_forward_staged") if _staged else (lib.msda_forward, "msda_forward"))
     with torch.cuda.device(dev):
         rc = fn(d.ref(), _ptr(value), _ptr(sampling_locations), _ptr(attention_weights), _ptr(out), _stream(dev))
     if rc != 0:
         raise MSDAError(rc, name)
     return out
+
+
+def msda_forward_staged(value, spatial_shapes, level_start_index, sampling_locations, attention_weights,
+                        value_layout: str = "BLNC", sampling_locations_layout: str = "BQHLP2",
+                        align_corners: bool = False, padding_mode: str = "zeros", out=None):
+    """msda_forward through the staged-level kernel: each thread block copies
+    the coarsest levels of its head that fit in shared memory there (TMA) and
+    gathers those levels' corners from it.  Same arguments and the same (bit
+    for bit) result as msda_forward; shapes the staged kernel does not cover
+    run msda_forward's kernel."""
+    return msda_forward(value, spatial_shapes, level_start_index, sampling_locations, attention_weights,
+                        value_layout, sampling_locations_layout, align_corners, padding_mode, out, _staged=True)
+
+
+def staged_levels(desc) -> int:
+    """First level msda_forward_staged stages for descriptor `desc` (from
+    make_desc); N_l when it runs msda_forward's kernel."""
+    lib = load_library()
+    n = ctypes.c_int(0)
+    rc = lib.msda_forward_staged_levels(desc.ref(), ctypes.byref(n))
+    if rc != 0:
+        raise MSDAError(rc, "msda_forward_staged_levels")
+    return int(n.value)
+
+
+def staged_timeouts() -> int:
+    """Staged-forward blocks (since the library was loaded) that gave up
+    waiting for their shared-memory copy; synchronises with the device."""
+    lib = load_library()
+    n = ctypes.c_uint(0)
+    rc = lib.msda_staged_timeouts(ctypes.byref(n))
+    if rc != 0:
+        raise MSDAError(rc, "msda_staged_timeouts")
+    return int(n.value)
 
 
 def msda_forward_logits(value, spatial_shapes, level_start_index, sampling_locations, attention_logits,

@@ -5,9 +5,13 @@
 #include "msda_entry.h"
 #include "msda_kernels.cuh"
 #include "msda_shape.cuh"
+#include "msda_staged.cuh"
 
+#include <cudaTypedefs.h>
 #include <limits.h>
 #include <string.h>
+
+#include <mutex>
 
 namespace {
 
@@ -251,6 +255,86 @@ BwdPlan plan_backward(const msda_desc *d, int compute_grad_value, bool allow_sor
     }
     w.total = end;
     return w;
+}
+
+// Staged-level forward (msda_forward_staged): the coarsest levels, from the
+// last one down, whose pixels of one head fit MSDA_STAGE_BYTES of shared
+// memory, each level's region rounded up to whole TMA boxes.  40 KB keeps
+// three blocks per SM; a 96 KB budget (two levels of the bfloat16 workloads,
+// two blocks per SM) measured slower.
+#ifndef MSDA_STAGE_BYTES
+#define MSDA_STAGE_BYTES (40 * 1024)
+#endif
+
+// false when the staged kernel does not apply (the direct forward runs):
+// 16-bit locations, scalar path or wide rows, a pixel row that is not a
+// multiple of 16 bytes, value not 16-byte aligned, or no level that fits.
+bool plan_stage(const msda_desc *d, const Config &cfg, const void *value, msda::StagePlan *sp, size_t *smem) {
+    const int64_t pxb = d->C_h * (int64_t)value_elem_size(d);  // bytes of one pixel of one head
+    if (d->loc_dtype != MSDA_DTYPE_F32 || !cfg.vec || !msda::specialised_shape(cfg.G, cfg.NCH) || pxb % 16 != 0 ||
+        d->C_h > 256 || !aligned(value, 16) || d->N_l < 1 || d->L < msda::kStageBox)
+        return false;
+    memset(sp, 0, sizeof(*sp));
+    sp->ls = (int)d->N_l;
+    int64_t pix = 0;
+    for (int64_t l = d->N_l - 1; l >= 0; --l) {
+        const int64_t n = d->spatial_shapes[2 * l] * d->spatial_shapes[2 * l + 1];
+        const int64_t region = (n + msda::kStageBox - 1) / msda::kStageBox * msda::kStageBox;
+        if ((pix + region) * pxb > MSDA_STAGE_BYTES) break;
+        pix += region;
+        sp->ls = (int)l;
+    }
+    if (sp->ls == (int)d->N_l) return false;
+    int64_t off = 0;
+    for (int64_t l = sp->ls; l < d->N_l; ++l) {
+        const int64_t n = d->spatial_shapes[2 * l] * d->spatial_shapes[2 * l + 1];
+        const int64_t region = (n + msda::kStageBox - 1) / msda::kStageBox * msda::kStageBox;
+        sp->sp[l] = (int)off;
+        off += region;
+        sp->boxes += (int)(region / msda::kStageBox);
+    }
+    sp->bytes = (uint32_t)(pix * pxb);
+    sp->layout = d->value_layout == MSDA_LAYOUT_BLNC ? 0 : 1;
+    *smem = (size_t)(pix * pxb) + 128;  // + slack for the kernel's 128-byte alignment
+    return true;
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link
+// against the driver library); null when the driver does not provide it.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+// value as a 4-D tensor, innermost first: (C_h, N_h, L, B) for (B, L, N_h, C_h)
+// or (C_h, L, N_h, B) for (B, N_h, L, C_h); a box is one head's channel rows of
+// kStageBox consecutive pixels.
+bool encode_value_map(const msda_desc *d, const void *value, CUtensorMap *tm) {
+    const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return false;
+    const cuuint64_t e = value_elem_size(d), C = (cuuint64_t)d->C_h, H = (cuuint64_t)d->N_h,
+                     L = (cuuint64_t)d->L, B = (cuuint64_t)d->B;
+    const bool blnc = d->value_layout == MSDA_LAYOUT_BLNC;
+    const cuuint64_t dims[4] = {C, blnc ? H : L, blnc ? L : H, B};
+    const cuuint64_t strides[3] = {C * e, (blnc ? H : L) * C * e, L * H * C * e};
+    const cuuint32_t box[4] = {(cuuint32_t)C, blnc ? 1u : (cuuint32_t)msda::kStageBox,
+                               blnc ? (cuuint32_t)msda::kStageBox : 1u, 1u};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    const CUresult r = enc(tm, d->value_dtype == MSDA_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                                : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                           4, const_cast<void *>(value), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
 }
 
 }  // namespace
@@ -538,8 +622,16 @@ int backward_entry(const msda_desc *desc, const void *grad_output, const void *v
     return record_cuda(e);
 }
 
+// Blocks of the staged forward that gave up waiting for their copy.
+__device__ unsigned int g_stage_timeouts = 0;
+
+int staged_timeouts(unsigned int *count) {
+    if (!count) return MSDA_ERR_NULL_POINTER;
+    return record_cuda(cudaMemcpyFromSymbol(count, g_stage_timeouts, sizeof(unsigned int)));
+}
+
 int forward_entry(const msda_desc *desc, const void *value, const void *sampling_locations,
-                  const void *attention_weights, void *out, bool logits, cudaStream_t stream) {
+                  const void *attention_weights, void *out, bool logits, bool staged, cudaStream_t stream) {
     int rc = validate_desc(desc);
     if (rc) return rc;
     const msda_desc *d = desc;
@@ -564,6 +656,27 @@ int forward_entry(const msda_desc *desc, const void *value, const void *sampling
     p.n_sm = sm_count();
     p.logits = logits ? 1 : 0;
     cudaError_t e;
+    StagePlan sp;
+    size_t smem = 0;
+    CUtensorMap tm;
+    if (staged && !logits && samples > 0 && plan_stage(d, cfg, value, &sp, &smem) &&
+        encode_value_map(d, value, &tm)) {
+        unsigned int *timeouts = nullptr;
+        e = cudaGetSymbolAddress((void **)&timeouts, g_stage_timeouts);
+        if (e == cudaSuccess) {
+            if (d->value_dtype == MSDA_DTYPE_F32)
+                e = launch_forward_staged<float>(p, sp, tm, smem, cfg.G, cfg.NCH, (const float *)value,
+                                                 (const float *)sampling_locations,
+                                                 (const float *)attention_weights, (float *)out, timeouts, stream);
+            else
+                e = launch_forward_staged<__nv_bfloat16>(p, sp, tm, smem, cfg.G, cfg.NCH,
+                                                         (const __nv_bfloat16 *)value,
+                                                         (const float *)sampling_locations,
+                                                         (const float *)attention_weights, (__nv_bfloat16 *)out,
+                                                         timeouts, stream);
+        }
+        return record_cuda(e);
+    }
     if (d->value_dtype == MSDA_DTYPE_F32)
         e = msda::launch_forward<float>(p, cfg.vec, cfg.G, cfg.NCH, (const float *)value,
                                         (const float *)sampling_locations, (const float *)attention_weights,
@@ -581,7 +694,28 @@ extern "C" {
 
 int msda_forward(const msda_desc *desc, const void *value, const void *sampling_locations,
                  const void *attention_weights, void *out, cudaStream_t stream) {
-    return msda::forward_entry(desc, value, sampling_locations, attention_weights, out, false, stream);
+    return msda::forward_entry(desc, value, sampling_locations, attention_weights, out, false, false, stream);
+}
+
+int msda_forward_staged(const msda_desc *desc, const void *value, const void *sampling_locations,
+                        const void *attention_weights, void *out, cudaStream_t stream) {
+    return msda::forward_entry(desc, value, sampling_locations, attention_weights, out, false, true, stream);
+}
+
+int msda_staged_timeouts(unsigned int *count) { return msda::staged_timeouts(count); }
+
+int msda_forward_staged_levels(const msda_desc *desc, int *first_level) {
+    if (!first_level) return MSDA_ERR_NULL_POINTER;
+    const int rc = validate_desc(desc);
+    if (rc) return rc;
+    Config cfg;
+    const int V = msda::VecWidth<float>::value;  // the same for both value dtypes
+    const int rc2 = choose_config(desc, V, true, MSDA_FWD_LANES, &cfg);
+    if (rc2) return rc2;
+    msda::StagePlan sp;
+    size_t smem;
+    *first_level = plan_stage(desc, cfg, (const void *)16, &sp, &smem) ? sp.ls : (int)desc->N_l;
+    return MSDA_OK;
 }
 
 size_t msda_backward_workspace_size(const msda_desc *desc, int compute_grad_value) {
@@ -612,7 +746,7 @@ int msda_backward_accumulate(const msda_desc *desc, const void *grad_output, con
 
 int msda_forward_logits(const msda_desc *desc, const void *value, const void *sampling_locations,
                         const void *attention_logits, void *out, cudaStream_t stream) {
-    return msda::forward_entry(desc, value, sampling_locations, attention_logits, out, true, stream);
+    return msda::forward_entry(desc, value, sampling_locations, attention_logits, out, true, false, stream);
 }
 
 int msda_backward_logits(const msda_desc *desc, const void *grad_output, const void *value,

@@ -29,8 +29,9 @@ int backward_entry(const msda_desc *desc, const void *grad_output, const void *v
                    void *grad_sampling_locations, void *grad_attention_weights, void *workspace,
                    size_t workspace_bytes, BwdMode mode, cudaStream_t stream);
 
-// msda_forward's argument checks and work; logits as in BwdMode.
+// msda_forward's argument checks and work; logits as in BwdMode; staged:
+// the staged-level kernel where it applies (msda_forward_staged).
 int forward_entry(const msda_desc *desc, const void *value, const void *sampling_locations,
-                  const void *attention_weights, void *out, bool logits, cudaStream_t stream);
+                  const void *attention_weights, void *out, bool logits, bool staged, cudaStream_t stream);
 
 }  // namespace msda

@@ -376,10 +376,11 @@ __device__ __forceinline__ float2 row_softmax_stats(const float *attn, int64_t a
 #endif
 // Blocks per SM the row kernels are compiled for, for rows of up to 8
 // elements a lane: the forward 4 (64 registers a thread: more warps to hide
-// the gather latency), the backward 3 (85 registers: its per-sample partials
-// and reduction need them); 2 (128 registers) for the wide-row kernels.
+// the gather latency) for one 4-element chunk a lane and 3 for two, the
+// backward 3 (85 registers: its per-sample partials and reduction need them);
+// 2 (128 registers) for the wide-row kernels.
 __host__ __device__ constexpr int row_min_blocks(int elems, bool fwd) {
-    return elems <= 8 ? (fwd ? MSDA_FWD_MIN_BLOCKS : MSDA_BWD_MIN_BLOCKS) : 2;
+    return elems <= 8 ? (fwd ? (elems <= 4 ? MSDA_FWD_MIN_BLOCKS : 3) : MSDA_BWD_MIN_BLOCKS) : 2;
 }
 
 // One sample's cell in the form the lanes of a group exchange (six 32-bit
@@ -468,7 +469,7 @@ msda_forward_kernel(const __grid_constant__ Params p, const T *__restrict__ valu
             }
             // consume phase: the group's samples in order, corners of two in flight
             const int ns = min(G, NLP - j0);
-            constexpr int S2 = (G >= 2 && NCH * VEC <= 8) ? 2 : 1;
+            constexpr int S2 = (G >= 2 && NCH * VEC <= 4) ? 2 : 1;  // two samples in flight for one chunk a lane
 #pragma unroll
             for (int s = 0; s < G; s += S2) {
                 if (s < ns) {

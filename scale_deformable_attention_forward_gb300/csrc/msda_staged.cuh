@@ -1,0 +1,239 @@
+// msda_staged.cuh -- the forward with staged coarse levels.
+//
+// The direct forward gathers every corner row through L1.  Here each block
+// serves a run of queries of one (b, h) and first copies the whole coarsest
+// levels of that head (as many as fit a shared-memory budget) into shared
+// memory with TMA tensor copies; samples on those levels gather from shared
+// memory, samples on the finer levels from global memory as before.  A coarse
+// level is small and hot (encoder32: level 3 of one head is 273 pixels, read
+// by about 30 corner lookups per pixel within one block), so the copy is paid
+// once per block and the gathers on it no longer depend on L1 hits.  The
+// arithmetic (cell, weights, order of the products and sums) is that of
+// msda_forward_kernel, so the two give bit-identical outputs.
+#pragma once
+
+#include <cuda.h>
+
+#include "msda_kernels.cuh"
+
+namespace msda {
+
+#ifndef MSDA_STAGED_MIN_BLOCKS
+#define MSDA_STAGED_MIN_BLOCKS 3  // 85 registers: the direct kernel's loop plus the staging state
+#endif
+
+constexpr int kStageBox = 32;                  // pixels per TMA box
+constexpr uint32_t kStageWaitLimit = 1u << 22;  // mbarrier polls before the block gives up on the copy
+
+// Staged levels ls..N_l-1 of one head: pixel i of level l sits at shared
+// pixel sp[l] + i (each level's region a whole number of boxes), C_h elements
+// per pixel.  The grid is B*N_h*bpb blocks; block k of (b, h) serves queries
+// [k*rpb, min(N_q, (k+1)*rpb)).
+struct StagePlan {
+    int ls;    // first staged level (N_l: none)
+    int bpb;   // blocks per (b, h)
+    int rpb;   // queries per block
+    int boxes; // TMA boxes per block
+    uint32_t bytes;  // bytes the boxes bring (the mbarrier's transaction count)
+    int layout;      // 0: value (B, L, N_h, C_h); 1: (B, N_h, L, C_h) -- the tensor map's dimension order
+    int sp[kMaxLevels];
+};
+
+template <typename T, int VEC> struct ShIO;
+template <> struct ShIO<float, 4> {
+    static __device__ __forceinline__ void load(uint32_t a, float (&o)[4]) {
+        asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                     : "=f"(o[0]), "=f"(o[1]), "=f"(o[2]), "=f"(o[3])
+                     : "r"(a));
+    }
+};
+template <> struct ShIO<__nv_bfloat16, 4> {
+    static __device__ __forceinline__ void load(uint32_t a, float (&o)[4]) {
+        uint32_t x, y;
+        asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(x), "=r"(y) : "r"(a));
+        o[0] = __uint_as_float(x << 16);
+        o[1] = __uint_as_float(x & 0xffff0000u);
+        o[2] = __uint_as_float(y << 16);
+        o[3] = __uint_as_float(y & 0xffff0000u);
+    }
+};
+
+__device__ __forceinline__ bool stage_wait(uint32_t bar, uint32_t phase) {
+    for (uint32_t it = 0; it < kStageWaitLimit; ++it) {
+        uint32_t done;
+        asm volatile(
+            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+            : "=r"(done)
+            : "r"(bar), "r"(phase)
+            : "memory");
+        if (done) return true;
+    }
+    return false;
+}
+
+// One block: stage, then the forward of its queries (the direct kernel's
+// loop, binary32 weights, specialised padding).  A block whose copy has not
+// landed after kStageWaitLimit polls counts itself in *timeouts and gathers
+// every level from global memory (same results), then waits for the copy
+// again (bounded) before it exits.
+template <typename T, int VEC, int G, int NCH, int PAD>
+__global__ void __launch_bounds__(kThreads, MSDA_STAGED_MIN_BLOCKS)
+msda_forward_staged_kernel(const __grid_constant__ Params p, const __grid_constant__ StagePlan sp,
+                           const __grid_constant__ CUtensorMap tmap, const T *__restrict__ value,
+                           const float *__restrict__ loc, const float *__restrict__ attn, T *__restrict__ out,
+                           unsigned int *__restrict__ timeouts) {
+    // dynamic shared memory: the staged pixels, from a 128-byte boundary (128 bytes of slack allocated)
+    extern __shared__ __align__(128) unsigned char stage_raw[];
+    __shared__ __align__(8) uint64_t bar_mem;
+    __shared__ LevelTables lt;
+    __shared__ int sps[kMaxLevels];
+    if (threadIdx.x < (unsigned)p.N_l) sps[threadIdx.x] = sp.sp[threadIdx.x];
+    load_level_tables(p, lt);  // (ends with __syncthreads)
+
+    const uint32_t bh = blockIdx.x / (uint32_t)sp.bpb;
+    const int q0 = (int)(blockIdx.x - bh * (uint32_t)sp.bpb) * sp.rpb;
+    const int q1 = min(p.N_q, q0 + sp.rpb);
+    if (q0 >= q1) return;  // uniform over the block
+    const uint32_t b = p.div_h.div(bh), h = bh - b * (uint32_t)p.N_h;
+
+    // stage: one thread arms the barrier with the boxes' bytes and issues them
+    const uint32_t bar = (uint32_t)__cvta_generic_to_shared(&bar_mem);
+    const uint32_t sbase = ((uint32_t)__cvta_generic_to_shared(stage_raw) + 127u) & ~127u;
+    const bool staging = sp.ls < p.N_l;
+    if (staging && threadIdx.x == 0) {
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(1) : "memory");
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(sp.bytes) : "memory");
+        const uint32_t box_bytes = (uint32_t)(kStageBox * p.C_h * (int)sizeof(T));
+        for (int l = sp.ls; l < p.N_l; ++l) {
+            const int npx = lt.H[l] * lt.W[l];
+            for (int i = 0; i * kStageBox < npx; ++i) {
+                const int px = lt.start[l] + i * kStageBox;  // first pixel of the box
+                const uint32_t dst = sbase + (uint32_t)(sps[l] + i * kStageBox) * (box_bytes / kStageBox);
+                // coordinates, innermost first: (channel, head, pixel, batch) or (channel, pixel, head, batch)
+                const int c1 = sp.layout == 0 ? (int)h : px, c2 = sp.layout == 0 ? px : (int)h;
+                asm volatile(
+                    "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+                    " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+                    "l"(reinterpret_cast<uint64_t>(&tmap)), "r"(0), "r"(c1), "r"(c2), "r"((int)b), "r"(bar)
+                    : "memory");
+            }
+        }
+    }
+    __syncthreads();  // the barrier is initialised before anyone polls it
+    const bool landed = staging ? stage_wait(bar, 0) : true;
+    const bool ok = __syncthreads_and(landed);
+    if (staging && !ok && threadIdx.x == 0) atomicAdd(timeouts, 1u);  // counted for msda_staged_timeouts()
+    const int lsj = (ok ? sp.ls : p.N_l) * p.N_p;  // samples j >= lsj gather from shared memory
+
+    constexpr int GPB = kThreads / G;
+    const int lane = threadIdx.x & 31;
+    const int r = lane & (G - 1);
+    const int base = lane & ~(G - 1);
+    const unsigned gmask = G == 32 ? 0xffffffffu : (((1u << G) - 1u) << base);
+    const int sP = p.v_sP, sJ = p.l_sJ, sXY = p.l_sXY, NLP = p.NLP, C = p.C_h;
+    int nk = 0;
+#pragma unroll
+    for (int k = 0; k < NCH; ++k) nk += (k * G + r < p.chunks);
+    const T *vbh = value + b * p.v_sB + (int64_t)h * p.v_sH + r * VEC;
+    const uint32_t sbr = sbase + (uint32_t)(r * VEC * (int)sizeof(T));  // this lane's channels of shared pixel 0
+
+    for (int q = q0 + (int)threadIdx.x / G; q < q1; q += GPB) {
+        const uint32_t bqh = (b * (uint32_t)p.N_q + (uint32_t)q) * (uint32_t)p.N_h + h;
+        const int64_t lo = b * p.l_sB + (int64_t)(((uint32_t)q * (uint32_t)p.N_h + h) * (uint32_t)NLP) * sJ;
+        const int64_t ao = (int64_t)bqh * NLP;
+        float acc[NCH][VEC];
+#pragma unroll
+        for (int k = 0; k < NCH; ++k)
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) acc[k][e] = 0.0f;
+
+        for (int j0 = 0; j0 < NLP; j0 += G) {
+            // owner phase: staged samples get offsets into shared memory (pixel stride C_h)
+            FwdCell mine = {0, 0, 0.0f, 0.0f, 0.0f, 0.0f};
+            const int j = j0 + r;
+            if (j < NLP) {
+                const float u = ldl(loc, lo + j * sJ, 0), v = ldl(loc, lo + j * sJ + sXY, 0);
+                const float A = ldl(attn, ao + j, 0);
+                const int l = (int)p.div_p.div((uint32_t)j);
+                const int W = lt.W[l], H = lt.H[l];
+                const Cell c = make_cell<PAD>(u, v, lt.sx[l], lt.sy[l], p.off, W, H, p.padding);
+                mine = j >= lsj ? fwd_cell(c, A, W, H, sps[l], C) : fwd_cell(c, A, W, H, lt.start[l], sP);
+            }
+            const int ns = min(G, NLP - j0);
+            constexpr int S2 = (G >= 2 && NCH * VEC <= 4) ? 2 : 1;  // two samples in flight for one chunk a lane
+#pragma unroll
+            for (int s = 0; s < G; s += S2) {
+                if (s < ns) {
+                    int o[S2][4];
+                    float w[S2][4];
+                    float x[S2][4][NCH][VEC];
+#pragma unroll
+                    for (int h2 = 0; h2 < S2; ++h2) {
+                        const int src = base + s + h2;
+                        const int o0 = __shfl_sync(gmask, mine.o0, src);
+                        const int o1 = __shfl_sync(gmask, mine.o1, src);
+                        const float ax0 = __shfl_sync(gmask, mine.ax0, src);
+                        const float ax1 = __shfl_sync(gmask, mine.ax1, src);
+                        const float ay0 = __shfl_sync(gmask, mine.ay0, src);
+                        const float ay1 = __shfl_sync(gmask, mine.ay1, src);
+                        // the same for every lane of the warp; a sample past the row's last
+                        // (weight 0, offset 0) reads global memory, as in the direct kernel
+                        const bool st = j0 + s + h2 >= lsj && j0 + s + h2 < NLP;
+                        const int dx = (int)((unsigned)o0 >> 31) * (st ? C : sP);
+                        o[h2][0] = o0 & 0x7fffffff;
+                        o[h2][1] = (o0 & 0x7fffffff) + dx;
+                        o[h2][2] = o1;
+                        o[h2][3] = o1 + dx;
+                        w[h2][0] = ay0 * ax0;
+                        w[h2][1] = ay0 * ax1;
+                        w[h2][2] = ay1 * ax0;
+                        w[h2][3] = ay1 * ax1;
+                        if (st) {
+#pragma unroll
+                            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                                for (int k = 0; k < NCH; ++k)
+                                    if (k < nk)
+                                        ShIO<T, VEC>::load(sbr + (uint32_t)(o[h2][i] + k * G * VEC) * (uint32_t)sizeof(T),
+                                                           x[h2][i][k]);
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                                for (int k = 0; k < NCH; ++k)
+                                    if (k < nk) VecIO<T, VEC>::load(vbh + o[h2][i] + k * G * VEC, x[h2][i][k]);
+                        }
+                    }
+#pragma unroll
+                    for (int h2 = 0; h2 < S2; ++h2)
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+#pragma unroll
+                            for (int k = 0; k < NCH; ++k)
+                                if (k < nk)
+#pragma unroll
+                                    for (int e = 0; e < VEC; ++e)
+                                        acc[k][e] = fmaf(w[h2][i], x[h2][i][k][e], acc[k][e]);
+                }
+            }
+        }
+        T *dst = out + (int64_t)bqh * C + r * VEC;
+#pragma unroll
+        for (int k = 0; k < NCH; ++k)
+            if (k < nk) VecIO<T, VEC>::store(dst + k * G * VEC, acc[k]);
+    }
+    // a copy that had not landed must not write into shared memory the next block owns
+    if (staging && !ok) stage_wait(bar, 0);
+}
+
+// Host side (msda_forward_staged_{f32,bf16}.cu): pick the kernel for (G, NCH,
+// padding), size the grid (blocks per (b, h) from the occupancy at `smem`
+// bytes) and launch.
+template <typename T>
+cudaError_t launch_forward_staged(const Params &p, StagePlan sp, const CUtensorMap &tmap, size_t smem, int G, int NCH,
+                                  const T *value, const float *loc, const float *attn, T *out,
+                                  unsigned int *timeouts, cudaStream_t stream);
+
+}  // namespace msda

@@ -62,6 +62,10 @@ def _fwd(lib, desc, value=FAKE, loc=FAKE, attn=FAKE, out=FAKE):
     return lib.msda_forward(desc.ref() if desc is not None else None, value, loc, attn, out, None)
 
 
+def _fwd_staged(lib, desc, value=FAKE, loc=FAKE, attn=FAKE, out=FAKE):
+    return lib.msda_forward_staged(desc.ref() if desc is not None else None, value, loc, attn, out, None)
+
+
 def _bwd(lib, desc, flags=(1, 1, 1), ws=None, ws_bytes=0, **ptrs):
     p = dict(go=FAKE, value=FAKE, loc=FAKE, attn=FAKE, gv=FAKE, gl=FAKE, ga=FAKE)
     p.update(ptrs)
@@ -70,8 +74,11 @@ def _bwd(lib, desc, flags=(1, 1, 1), ws=None, ws_bytes=0, **ptrs):
 
 
 @no_gpu
-def test_rejections_forward(lib):
+@pytest.mark.parametrize("entry", ["msda_forward", "msda_forward_staged"])
+def test_rejections_forward(lib, entry):
+    """Both forward entry points validate the same way."""
     d = msda.make_desc
+    _fwd = globals()["_fwd_staged" if entry == "msda_forward_staged" else "_fwd"]
     assert _fwd(lib, None) == -1
     assert _fwd(lib, d(DIMS, LEVELS, STARTS), out=None) == -1
     assert _fwd(lib, d(DIMS, LEVELS, STARTS), value=None) == -1
@@ -145,3 +152,54 @@ def test_python_binding_rejects_cpu_tensors(lib):
         msda.msda_forward(v, LEVELS, STARTS, loc, a)
     with pytest.raises(ValueError):
         msda.msda_backward(torch.zeros(1, 2, 4), v, LEVELS, STARTS, loc, a)
+
+
+def test_staged_timeouts_rejects_null(lib):
+    assert lib.msda_staged_timeouts(None) == -1
+
+
+def _staged_levels(w, **over):
+    from scale_deformable_attention_forward_gb300 import inputs as gen
+    kw = dict(value_layout=w.value_layout, sampling_locations_layout=w.loc_layout, align_corners=w.align_corners,
+              padding_mode=w.padding_mode, value_dtype=msda.DTYPE_BF16 if w.dtype == "bf16" else msda.DTYPE_F32)
+    kw.update(over)
+    dims = over.pop("dims", None) or (w.B, w.n_queries, w.N_h, w.C_h, w.N_l, w.N_p, w.L)
+    kw.pop("dims", None)
+    return msda.staged_levels(msda.make_desc(dims, w.levels, w.level_start_index, **kw))
+
+
+def test_staged_level_choice():
+    """The coarsest levels whose pixels of one head fit 40 KB, each rounded up
+    to whole 32-pixel boxes: level 3 only for every workload (encoder32,
+    binary32 at 128 B a pixel: 288 px = 36 KB, with level 2 1344 px = 168 KB;
+    the bfloat16 workloads at 64 B a pixel: 18 KB and 16 KB, with level 2
+    84 KB and 80 KB)."""
+    from scale_deformable_attention_forward_gb300 import inputs as gen
+    W = gen.WORKLOADS
+    assert _staged_levels(W["encoder32"]) == 3
+    assert _staged_levels(W["decoder"]) == 3
+    assert _staged_levels(W["encoder16"]) == 3
+    assert _staged_levels(W["hires16"]) == 3
+    w = W["encoder32"]
+    N_l = w.N_l
+    assert _staged_levels(w, loc_dtype=msda.DTYPE_BF16) == N_l  # 16-bit locations: the direct kernel
+    B, N_q, N_h, C_h, _, N_p, L = w.B, w.n_queries, w.N_h, w.C_h, w.N_l, w.N_p, w.L
+    assert _staged_levels(w, dims=(B, N_q, N_h, 5, N_l, N_p, L)) == N_l    # scalar path
+    assert _staged_levels(w, dims=(B, N_q, N_h, 96, N_l, N_p, L)) == N_l   # wide rows
+    assert _staged_levels(w, dims=(B, N_q, N_h, 64, N_l, N_p, L)) == N_l   # 288 px x 256 B = 72 KB: none fits
+    assert _staged_levels(w, dims=(B, N_q, N_h, 32, N_l, N_p, L), value_dtype=msda.DTYPE_BF16) == 3
+    assert _staged_levels(w, dims=(B, N_q, N_h, 4, N_l, N_p, L), value_dtype=msda.DTYPE_BF16) == N_l  # 8-byte rows
+    # 16-byte pixels: levels 2-3 fit (1344 px = 21 KB), with level 1 87 KB
+    assert _staged_levels(w, dims=(B, N_q, N_h, 8, N_l, N_p, L), value_dtype=msda.DTYPE_BF16) == 2
+    one = msda.make_desc((1, 4, 1, 32, 1, 1, 40000), ((200, 200),), (0,))
+    assert msda.staged_levels(one) == 1  # 5 MB: no level fits
+    small = msda.make_desc((1, 4, 1, 32, 1, 1, 20), ((4, 5),), (0,))
+    assert msda.staged_levels(small) == 1  # L < 32 pixels
+
+
+def test_staged_levels_rejects_bad_input(lib):
+    d = msda.make_desc(DIMS, LEVELS, STARTS)
+    assert lib.msda_forward_staged_levels(d.ref(), None) == -1
+    bad = msda.make_desc(DIMS, LEVELS, (1, 24))
+    n = ctypes.c_int(0)
+    assert lib.msda_forward_staged_levels(bad.ref(), ctypes.byref(n)) == -5
