@@ -384,6 +384,29 @@ def run_ours(args, w: gen.Workload):
     staged_first = msda.staged_levels(desc)
     staged_timeouts = msda.staged_timeouts()
 
+    # The backward with per-level shared-memory grad_value accumulation
+    # (msda_backward_staged), same protocol, outside the step.
+    gv_st, gl_st, ga_st = torch.empty_like(gv), torch.empty_like(gl), torch.empty_like(ga)
+
+    def bwd_staged():
+        msda.msda_backward_staged(t["grad_output"], t["value"], data["spatial_shapes"], data["level_start_index"],
+                                  t["sampling_locations"], t["attention_weights"], grad_value=gv_st,
+                                  grad_sampling_locations=gl_st, grad_attention_weights=ga_st, workspace=ws, **kw)
+
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        bwd_staged()
+    ev_sb = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    for i in range(K):
+        flush.fill_(float(i))
+        ev_sb[i][0].record(stream)
+        bwd_staged()
+        ev_sb[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    staged_bwd_ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in ev_sb), world, dev)
+    staged_bwd_same = bool(torch.equal(gl_st, gl) and torch.equal(ga_st, ga))
+    staged_bwd_first = msda.backward_staged_levels(desc)
+
     # End to end: pinned host inputs -> device, forward, backward, results ->
     # pinned host, every step.  Two buffer sets and three streams pipeline the
     # steps the way a production loop would: the inputs of step i+1 are copied
@@ -505,6 +528,12 @@ def run_ours(args, w: gen.Workload):
             "speedup_vs_direct": round(fwd_mean / staged_ms, 4) if staged_ms > 0 else None,
             "staged_levels": list(range(staged_first, w.N_l)), "bit_identical_to_direct": staged_same,
             "timeouts": staged_timeouts},
+        "backward_staged": {
+            "what": "msda_backward_staged: grad_value of the coarse levels accumulated per block in shared memory",
+            "bwd_ms": round(staged_bwd_ms, 6), "direct_bwd_ms": round(bwd_mean, 6),
+            "speedup_vs_direct": round(bwd_mean / staged_bwd_ms, 4) if staged_bwd_ms > 0 else None,
+            "staged_levels": list(range(staged_bwd_first, w.N_l)),
+            "loc_attn_grads_bit_identical_to_direct": staged_bwd_same},
         "roofline_step": {
             "what": "forward + backward compulsory bytes / step time",
             "achieved": round((fwd_b + bwd_b) / (step_ms * 1e-3) / 1e9, 1), "peak": peak, "unit": "GB/s",

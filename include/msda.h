@@ -163,6 +163,33 @@ int msda_staged_timeouts(unsigned int *count);
  * Returns MSDA_OK or the descriptor's validation status. */
 int msda_forward_staged_levels(const msda_desc *desc, int *first_level);
 
+/* The backward with a per-level shared-memory grad_value accumulator (the
+ * same operation as msda_backward: "MS Deformable Attention Backward Kernel
+ * API Reference", Parameters and Returns; the page scatters grad_value into
+ * several HBM buffers, and a per-block accumulator is the GPU counterpart).
+ * Each thread block serves a run of queries of one (b, h) and keeps a
+ * binary32 accumulator for the coarsest levels of that head whose pixels fit
+ * 40 KB of shared memory; samples on those levels add their corner
+ * contributions there, samples on finer levels straight into grad_value's
+ * accumulator, and the block adds its shared rows in at its end.
+ * grad_sampling_locations and grad_attention_weights are bit-identical to
+ * msda_backward's; grad_value equals it up to summation order.  Arguments,
+ * workspace size, ownership and errors are msda_backward's.  Applies when
+ * grad_value is requested with C_h a multiple of 4 and at most 64 and
+ * 16-byte aligned tensors; otherwise msda_backward's kernels run. */
+int msda_backward_staged(const msda_desc *desc, const void *grad_output, const void *value,
+                         const void *sampling_locations, const void *attention_weights,
+                         int compute_grad_value, int compute_grad_sampling_locations,
+                         int compute_grad_attention_weights, void *grad_value,
+                         void *grad_sampling_locations, void *grad_attention_weights, void *workspace,
+                         size_t workspace_bytes, cudaStream_t stream);
+
+/* The first level msda_backward_staged accumulates in shared memory for this
+ * descriptor (N_l when it runs msda_backward's kernels), assuming aligned
+ * tensors and grad_value requested.  Host only.  Returns MSDA_OK or the
+ * descriptor's validation status. */
+int msda_backward_staged_levels(const msda_desc *desc, int *first_level);
+
 /* Bytes of device workspace msda_backward needs, 0 when compute_grad_value is
  * 0.  With compute_grad_value set it is the sum of (each part starting at a
  * 256-byte boundary of the workspace):

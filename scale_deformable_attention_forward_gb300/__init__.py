@@ -91,6 +91,10 @@ def load_library() -> ctypes.CDLL:
             lib.msda_staged_timeouts.restype = I
             lib.msda_forward_staged_levels.argtypes = [D, ctypes.POINTER(ctypes.c_int)]
             lib.msda_forward_staged_levels.restype = I
+            lib.msda_backward_staged.argtypes = [D, P, P, P, P, I, I, I, P, P, P, P, Z, P]
+            lib.msda_backward_staged.restype = I
+            lib.msda_backward_staged_levels.argtypes = [D, ctypes.POINTER(ctypes.c_int)]
+            lib.msda_backward_staged_levels.restype = I
             lib.msda_backward_logits.argtypes = [D, P, P, P, P, I, I, I, P, P, P, P, Z, P]
             lib.msda_backward_logits.restype = I
             lib.msda_status_string.argtypes = [I]
@@ -320,7 +324,8 @@ def msda_backward(grad_output, value, spatial_shapes, level_start_index, samplin
                   align_corners: bool = False, padding_mode: str = "zeros", compute_grad_value: bool = True,
                   compute_grad_sampling_locations: bool = True, compute_grad_attention_weights: bool = True,
                   grad_value=None, grad_sampling_locations=None, grad_attention_weights=None,
-                  workspace=None, _accumulate: bool = False, _logits: bool = False) -> Tuple:
+                  workspace=None, _accumulate: bool = False, _logits: bool = False,
+                  _staged: bool = False) -> Tuple:
     """Multi-scale deformable attention backward on the GPU.
 
     Returns (grad_value, grad_sampling_locations, grad_attention_weights);
@@ -386,15 +391,45 @@ def msda_backward(grad_output, value, spatial_shapes, level_start_index, samplin
             raise ValueError(f"workspace must hold {ws_bytes} bytes on {dev}")
     with torch.cuda.device(dev):
         fn = (lib.msda_backward_accumulate if _accumulate else
-              lib.msda_backward_logits if _logits else lib.msda_backward)
+              lib.msda_backward_logits if _logits else
+              lib.msda_backward_staged if _staged else lib.msda_backward)
         rc = fn(d.ref(), _ptr(grad_output), _ptr(value), _ptr(sampling_locations),
                                _ptr(attention_weights), int(fv), int(fl), int(fa), _ptr(grad_value),
                                _ptr(grad_sampling_locations), _ptr(grad_attention_weights),
                                _ptr(workspace) if ws_bytes > 0 else None, ws_bytes, _stream(dev))
     if rc != 0:
         raise MSDAError(rc, "msda_backward_accumulate" if _accumulate else
-                        "msda_backward_logits" if _logits else "msda_backward")
+                        "msda_backward_logits" if _logits else
+                        "msda_backward_staged" if _staged else "msda_backward")
     return grad_value, grad_sampling_locations, grad_attention_weights
+
+
+def msda_backward_staged(grad_output, value, spatial_shapes, level_start_index, sampling_locations,
+                         attention_weights, value_layout: str = "BLNC", sampling_locations_layout: str = "BQHLP2",
+                         align_corners: bool = False, padding_mode: str = "zeros", compute_grad_value: bool = True,
+                         compute_grad_sampling_locations: bool = True, compute_grad_attention_weights: bool = True,
+                         grad_value=None, grad_sampling_locations=None, grad_attention_weights=None,
+                         workspace=None) -> Tuple:
+    """msda_backward with grad_value of the coarse levels accumulated per
+    thread block in shared memory (then added in once per block); the same
+    arguments and results (grad_value up to summation order)."""
+    return msda_backward(grad_output, value, spatial_shapes, level_start_index, sampling_locations,
+                         attention_weights, value_layout, sampling_locations_layout, align_corners, padding_mode,
+                         compute_grad_value, compute_grad_sampling_locations, compute_grad_attention_weights,
+                         grad_value=grad_value, grad_sampling_locations=grad_sampling_locations,
+                         grad_attention_weights=grad_attention_weights, workspace=workspace, _staged=True)
+
+
+def backward_staged_levels(desc) -> int:
+    """First level msda_backward_staged accumulates in shared memory for
+    descriptor `desc` (from make_desc); N_l when it runs msda_backward's
+    kernels."""
+    lib = load_library()
+    n = ctypes.c_int(0)
+    rc = lib.msda_backward_staged_levels(desc.ref(), ctypes.byref(n))
+    if rc != 0:
+        raise MSDAError(rc, "msda_backward_staged_levels")
+    return int(n.value)
 
 
 

@@ -24,7 +24,7 @@ SOURCES = ["msda_api.cu", "msda_noalloc.cu"] + [
     f"msda_forward_{t}_{path}.cu" for t in ("f32", "bf16") for path in ("vector", "scalar")] + [
     f"msda_backward_{t}_{pad}.cu" for t in ("f32", "bf16") for pad in ("zeros", "border", "wide", "scalar")] + [
     f"msda_tile_reduce_{t}.cu" for t in ("f32", "bf16")] + [
-    f"msda_forward_staged_{t}.cu" for t in ("f32", "bf16")]
+    f"msda_staged_{t}.cu" for t in ("f32", "bf16")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
 

@@ -269,11 +269,9 @@ BwdPlan plan_backward(const msda_desc *d, int compute_grad_value, bool allow_sor
 // false when the staged kernel does not apply (the direct forward runs):
 // 16-bit locations, scalar path or wide rows, a pixel row that is not a
 // multiple of 16 bytes, value not 16-byte aligned, or no level that fits.
-bool plan_stage(const msda_desc *d, const Config &cfg, const void *value, msda::StagePlan *sp, size_t *smem) {
-    const int64_t pxb = d->C_h * (int64_t)value_elem_size(d);  // bytes of one pixel of one head
-    if (d->loc_dtype != MSDA_DTYPE_F32 || !cfg.vec || !msda::specialised_shape(cfg.G, cfg.NCH) || pxb % 16 != 0 ||
-        d->C_h > 256 || !aligned(value, 16) || d->N_l < 1 || d->L < msda::kStageBox)
-        return false;
+// The levels themselves: from the last one down while their pixels of one
+// head (pxb bytes each) fit the budget.
+bool plan_levels(const msda_desc *d, int64_t pxb, msda::StagePlan *sp, size_t *smem) {
     memset(sp, 0, sizeof(*sp));
     sp->ls = (int)d->N_l;
     int64_t pix = 0;
@@ -295,7 +293,27 @@ bool plan_stage(const msda_desc *d, const Config &cfg, const void *value, msda::
     }
     sp->bytes = (uint32_t)(pix * pxb);
     sp->layout = d->value_layout == MSDA_LAYOUT_BLNC ? 0 : 1;
-    *smem = (size_t)(pix * pxb) + 128;  // + slack for the kernel's 128-byte alignment
+    *smem = (size_t)(pix * pxb);
+    return true;
+}
+
+bool plan_stage(const msda_desc *d, const Config &cfg, const void *value, msda::StagePlan *sp, size_t *smem) {
+    const int64_t pxb = d->C_h * (int64_t)value_elem_size(d);  // bytes of one pixel of one head
+    if (d->loc_dtype != MSDA_DTYPE_F32 || !cfg.vec || !msda::specialised_shape(cfg.G, cfg.NCH) || pxb % 16 != 0 ||
+        d->C_h < 4 || d->C_h > 256 || !aligned(value, 16) || d->N_l < 1 || d->L < msda::kStageBox)
+        return false;
+    if (!plan_levels(d, pxb, sp, smem)) return false;
+    *smem += 128;  // slack for the kernel's 128-byte alignment of the TMA destinations
+    return true;
+}
+
+// msda_backward_staged: the binary32 grad_value accumulator of the staged
+// levels (C_h * 4 bytes a pixel), the vector path's specialised shapes.
+bool plan_stage_backward(const msda_desc *d, const Config &cfg, msda::StagePlan *sp, size_t *smem) {
+    if (!cfg.vec || !msda::specialised_shape(cfg.G, cfg.NCH) || d->C_h < 4 || d->N_l < 1) return false;
+    if (!plan_levels(d, d->C_h * 4, sp, smem)) return false;
+    const int chunks = (int)(d->C_h / 4);
+    sp->rot = (chunks & (chunks - 1)) == 0 ? (chunks < 8 ? chunks : 8) - 1 : 0;
     return true;
 }
 
@@ -594,6 +612,29 @@ int backward_entry(const msda_desc *desc, const void *grad_output, const void *v
 
     cudaError_t e = cudaSuccess;
     if (fv && !accumulate) e = launch_zero_f32(bb.gv_acc, value_elems, stream);
+    // staged variant (msda_backward_staged): the per-level shared-memory
+    // accumulator kernel in place of the row kernel, where it applies
+    StagePlan sp;
+    size_t smem = 0;
+    const bool staged = mode.staged && fv && !mode.logits && samples > 0 && plan_stage_backward(d, cfg, &sp, &smem);
+    if (staged) {
+        if (e == cudaSuccess) {
+            if (bf16)
+                e = launch_backward_staged<__nv_bfloat16>(p, sp, smem, cfg.G, cfg.NCH,
+                                                          (const __nv_bfloat16 *)grad_output,
+                                                          (const __nv_bfloat16 *)value, (const float *)sampling_locations,
+                                                          (const float *)attention_weights, bb.gv_acc, bb.grad_loc,
+                                                          bb.grad_attn, stream);
+            else
+                e = launch_backward_staged<float>(p, sp, smem, cfg.G, cfg.NCH, (const float *)grad_output,
+                                                  (const float *)value, (const float *)sampling_locations,
+                                                  (const float *)attention_weights, bb.gv_acc, bb.grad_loc,
+                                                  bb.grad_attn, stream);
+        }
+        if (e == cudaSuccess && bf16 && !accumulate)
+            e = launch_f32_to_bf16(bb.gv_acc, (__nv_bfloat16 *)grad_value, value_elems, stream);
+        return record_cuda(e);
+    }
     // tile-sorted grad_value (vector path): partition, the row kernel for the
     // other two gradients only, then the per-tile reduction
     const bool sort = plan.sort && cfg.vec && !fl && !fa;
@@ -703,6 +744,32 @@ int msda_forward_staged(const msda_desc *desc, const void *value, const void *sa
 }
 
 int msda_staged_timeouts(unsigned int *count) { return msda::staged_timeouts(count); }
+
+int msda_backward_staged(const msda_desc *desc, const void *grad_output, const void *value,
+                         const void *sampling_locations, const void *attention_weights, int compute_grad_value,
+                         int compute_grad_sampling_locations, int compute_grad_attention_weights, void *grad_value,
+                         void *grad_sampling_locations, void *grad_attention_weights, void *workspace,
+                         size_t workspace_bytes, cudaStream_t stream) {
+    msda::BwdMode mode{true, false, false};
+    mode.staged = true;
+    return msda::backward_entry(desc, grad_output, value, sampling_locations, attention_weights, compute_grad_value,
+                                compute_grad_sampling_locations, compute_grad_attention_weights, grad_value,
+                                grad_sampling_locations, grad_attention_weights, workspace, workspace_bytes, mode,
+                                stream);
+}
+
+int msda_backward_staged_levels(const msda_desc *desc, int *first_level) {
+    if (!first_level) return MSDA_ERR_NULL_POINTER;
+    const int rc = validate_desc(desc);
+    if (rc) return rc;
+    Config cfg;
+    const int rc2 = choose_config(desc, msda::BwdVecWidth<float>::value, true, MSDA_BWD_LANES, &cfg);
+    if (rc2) return rc2;
+    msda::StagePlan sp;
+    size_t smem;
+    *first_level = plan_stage_backward(desc, cfg, &sp, &smem) ? sp.ls : (int)desc->N_l;
+    return MSDA_OK;
+}
 
 int msda_forward_staged_levels(const msda_desc *desc, int *first_level) {
     if (!first_level) return MSDA_ERR_NULL_POINTER;

@@ -17,9 +17,12 @@ size_t backward_workspace_bytes(const msda_desc *desc, int compute_grad_value, b
 //               without zeroing and without conversion;
 //   logits      attention_weights holds logits (softmax over each row's
 //               N_l*N_p slots gives the weights) and grad_attention_weights
-//               receives the logits' gradient.
+//               receives the logits' gradient;
+//   staged      grad_value of the coarse levels accumulated per block in
+//               shared memory where that kernel applies (msda_backward_staged).
 struct BwdMode {
     bool allow_sort, accumulate, logits;
+    bool staged = false;
 };
 
 // msda_backward's argument checks and work, in the given mode.

@@ -374,13 +374,13 @@ __device__ __forceinline__ float2 row_softmax_stats(const float *attn, int64_t a
 #ifndef MSDA_BWD_MIN_BLOCKS
 #define MSDA_BWD_MIN_BLOCKS 3
 #endif
-// Blocks per SM the row kernels are compiled for, for rows of up to 8
-// elements a lane: the forward 4 (64 registers a thread: more warps to hide
-// the gather latency) for one 4-element chunk a lane and 3 for two, the
-// backward 3 (85 registers: its per-sample partials and reduction need them);
-// 2 (128 registers) for the wide-row kernels.
+// Blocks per SM the row kernels are compiled for: for one 4-element chunk a
+// lane the forward 4 (64 registers a thread: more warps to hide the gather
+// latency) and the backward 3 (85 registers: its per-sample partials and
+// reduction need them); for two chunks the forward 3 and the backward 2; 2
+// (128 registers) for the wide-row kernels.
 __host__ __device__ constexpr int row_min_blocks(int elems, bool fwd) {
-    return elems <= 8 ? (fwd ? (elems <= 4 ? MSDA_FWD_MIN_BLOCKS : 3) : MSDA_BWD_MIN_BLOCKS) : 2;
+    return elems <= 4 ? (fwd ? MSDA_FWD_MIN_BLOCKS : MSDA_BWD_MIN_BLOCKS) : (elems <= 8 && fwd) ? 3 : 2;
 }
 
 // One sample's cell in the form the lanes of a group exchange (six 32-bit

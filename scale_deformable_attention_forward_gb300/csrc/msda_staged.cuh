@@ -36,6 +36,7 @@ struct StagePlan {
     int boxes; // TMA boxes per block
     uint32_t bytes;  // bytes the boxes bring (the mbarrier's transaction count)
     int layout;      // 0: value (B, L, N_h, C_h); 1: (B, N_h, L, C_h) -- the tensor map's dimension order
+    int rot;         // backward: channel-chunk rotation mask of the shared accumulator (0: none)
     int sp[kMaxLevels];
 };
 
@@ -228,12 +229,241 @@ msda_forward_staged_kernel(const __grid_constant__ Params p, const __grid_consta
     if (staging && !ok) stage_wait(bar, 0);
 }
 
-// Host side (msda_forward_staged_{f32,bf16}.cu): pick the kernel for (G, NCH,
+// ---------------------------------------------------------------- staged backward
+// The backward with a per-level shared-memory grad_value accumulator (the
+// alternative to direct atomics for the coarse levels): each block serves a
+// run of queries of one (b, h) and keeps a binary32 accumulator for the
+// staged levels of that head in shared memory.  Samples on those levels add
+// their four corner contributions there (red.shared.add.f32), samples on
+// finer levels straight into the global accumulator as in
+// msda_backward_kernel; at the end the block adds its shared rows into the
+// global accumulator (red.global.add.v4.f32, rows that stayed zero skipped).
+// grad_sampling_locations and grad_attention_weights are the direct kernel's
+// (the same record exchange, gathers and reductions), so they are
+// bit-identical to msda_backward's.  Channel chunk c of staged pixel x sits
+// at chunk (c + (x & rot)) & (chunks - 1) of the pixel's row (chunks a power
+// of two; rot = 0 otherwise), so that the groups of a warp, usually on
+// different pixels, spread over the banks.
+__device__ __forceinline__ void red_shared_add(uint32_t a, float v) {
+    asm volatile("red.shared.add.f32 [%0], %1;" ::"r"(a), "f"(v) : "memory");
+}
+
+template <typename T, int VEC, int G, int NCH, int PAD>
+__global__ void __launch_bounds__(kThreads, NCH == 1 ? MSDA_BWD_MIN_BLOCKS : 2)
+msda_backward_staged_kernel(const __grid_constant__ Params p, const __grid_constant__ StagePlan sp,
+                            const T *__restrict__ grad_out, const T *__restrict__ value,
+                            const float *__restrict__ loc, const float *__restrict__ attn,
+                            float *__restrict__ gv_acc, float *__restrict__ grad_loc, float *__restrict__ grad_attn) {
+    extern __shared__ __align__(16) float acc_s[];  // staged pixels x C_h, binary32
+    __shared__ LevelTables lt;
+    __shared__ int4 rec_o[kThreads];
+    __shared__ float4 rec_w[kThreads];
+    __shared__ int4 rec_s[kThreads];  // staged samples: the corners' staged pixel indices
+    __shared__ int sps[kMaxLevels];
+    if (threadIdx.x < (unsigned)p.N_l) sps[threadIdx.x] = sp.sp[threadIdx.x];
+    load_level_tables(p, lt);
+
+    const uint32_t bh = blockIdx.x / (uint32_t)sp.bpb;
+    const int q0 = (int)(blockIdx.x - bh * (uint32_t)sp.bpb) * sp.rpb;
+    const int q1 = min(p.N_q, q0 + sp.rpb);
+    if (q0 >= q1) return;  // uniform over the block
+    const uint32_t b = p.div_h.div(bh), h = bh - b * (uint32_t)p.N_h;
+    const int C = p.C_h, npix = sp.boxes * kStageBox;
+    for (int i = threadIdx.x; i < npix * C; i += kThreads) acc_s[i] = 0.0f;
+    __syncthreads();
+
+    constexpr int GPB = kThreads / G;
+    const int flags = p.flags;
+    const bool want_gl = flags & kGradLoc, want_ga = flags & kGradAttn;
+    const bool need_v = want_gl || want_ga;
+    const int lane = threadIdx.x & 31;
+    const int r = lane & (G - 1);
+    const int grp = lane / G;
+    const unsigned gmask = G == 32 ? 0xffffffffu : (((1u << G) - 1u) << (lane & ~(G - 1)));
+    int4 *wo = rec_o + (threadIdx.x & ~31);
+    float4 *ww = rec_w + (threadIdx.x & ~31);
+    int4 *wsx = rec_s + (threadIdx.x & ~31);
+    const int mypos = rec_pos<G>(grp, r);
+    const int sP = p.v_sP, sJ = p.l_sJ, sXY = p.l_sXY, NLP = p.NLP;
+    const int lsj = sp.ls * p.N_p;  // samples j >= lsj accumulate in shared memory
+    int nk = 0;
+#pragma unroll
+    for (int k = 0; k < NCH; ++k) nk += (k * G + r < p.chunks);
+    const int64_t bhoff = b * p.v_sB + (int64_t)h * p.v_sH;
+    const T *vbh = value + bhoff + r * VEC;
+    float *gbh = gv_acc + bhoff + r * VEC;
+    const uint32_t sacc = (uint32_t)__cvta_generic_to_shared(acc_s);
+
+    for (int q = q0 + (int)threadIdx.x / G; q < q1; q += GPB) {
+        const uint32_t bqh = (b * (uint32_t)p.N_q + (uint32_t)q) * (uint32_t)p.N_h + h;
+        const int64_t lrow = b * p.l_sB + (int64_t)(((uint32_t)q * (uint32_t)p.N_h + h) * (uint32_t)NLP) * sJ;
+        const int64_t ao = (int64_t)bqh * NLP;
+        float g[NCH][VEC];
+        {
+            const T *src = grad_out + (int64_t)bqh * C + r * VEC;
+#pragma unroll
+            for (int k = 0; k < NCH; ++k) {
+                if (k < nk) {
+                    VecIO<T, VEC>::load(src + k * G * VEC, g[k]);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e) g[k][e] = 0.0f;
+                }
+            }
+        }
+        for (int j0 = 0; j0 < NLP; j0 += G) {
+            const int j = j0 + r;
+            const bool live = j < NLP;
+            int l = 0;
+            float A = 0.0f;
+            Cell c;
+            {
+                Corners cr = {{0, 0, 0, 0}, {0.0f, 0.0f, 0.0f, 0.0f}};
+                float u = 0.0f, v = 0.0f;
+                if (live) {
+                    l = (int)p.div_p.div((uint32_t)j);
+                    u = ldl(loc, lrow + j * sJ, p.loc_dt);
+                    v = ldl(loc, lrow + j * sJ + sXY, p.loc_dt);
+                    A = ldl(attn, ao + j, p.loc_dt);
+                }
+                const int W = lt.W[l], H = lt.H[l];
+                c = make_cell<PAD>(u, v, lt.sx[l], lt.sy[l], p.off, W, H, p.padding);
+                if (live) cr = corners_of(c, A, W, H, lt.start[l], sP);
+                wo[mypos] = make_int4(cr.o[0], cr.o[1], cr.o[2], cr.o[3]);
+                ww[mypos] = make_float4(cr.w[0], cr.w[1], cr.w[2], cr.w[3]);
+                if (live && j >= lsj) {  // the same corners as staged pixel indices (stride 1)
+                    const Corners cs = corners_of(c, A, W, H, sps[l], 1);
+                    wsx[mypos] = make_int4(cs.o[0], cs.o[1], cs.o[2], cs.o[3]);
+                }
+            }
+            __syncwarp(gmask);
+            const int ns = min(G, NLP - j0);
+            float pd[4][G <= 8 ? G : 1];
+            float dt[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+            for (int s = 0; s < G; ++s) {
+                float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                if (s < ns) {
+                    const int qp = rec_pos<G>(grp, s);
+                    const int4 o4 = wo[qp];
+                    const int oo[4] = {o4.x, o4.y, o4.z, o4.w};
+                    if (need_v) {
+                        float x[4][NCH][VEC];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+#pragma unroll
+                            for (int k = 0; k < NCH; ++k)
+                                if (k < nk) VecIO<T, VEC>::load(vbh + oo[i] + k * G * VEC, x[i][k]);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+#pragma unroll
+                            for (int k = 0; k < NCH; ++k)
+                                if (k < nk)
+#pragma unroll
+                                    for (int e = 0; e < VEC; ++e) d[i] = fmaf(g[k][e], x[i][k][e], d[i]);
+                    }
+                    const float4 w4 = ww[qp];
+                    const float wv[4] = {w4.x, w4.y, w4.z, w4.w};
+                    if (j0 + s >= lsj) {  // staged level (the same for every lane of the warp)
+                        const int4 s4 = wsx[qp];
+                        const int px[4] = {s4.x, s4.y, s4.z, s4.w};
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            if (wv[i] != 0.0f)
+#pragma unroll
+                                for (int k = 0; k < NCH; ++k)
+                                    if (k < nk) {
+                                        const int ck = ((k * G + r) + (px[i] & sp.rot)) & (p.chunks - 1);
+                                        const int cc = sp.rot ? ck : k * G + r;
+                                        const uint32_t a = sacc + (uint32_t)((px[i] * C + cc * VEC) * 4);
+#pragma unroll
+                                        for (int e = 0; e < VEC; ++e) red_shared_add(a + 4 * e, wv[i] * g[k][e]);
+                                    }
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            if (wv[i] != 0.0f)
+#pragma unroll
+                                for (int k = 0; k < NCH; ++k)
+                                    if (k < nk) RedIO<VEC>::add(gbh + oo[i] + k * G * VEC, g[k], wv[i]);
+                    }
+                }
+                if constexpr (G <= 8) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) pd[i][s] = d[i];
+                } else if (need_v) {
+#pragma unroll
+                    for (int o = 1; o < G; o <<= 1)
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) d[i] += __shfl_xor_sync(gmask, d[i], o);
+                    if (r == s) {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) dt[i] = d[i];
+                    }
+                }
+            }
+            __syncwarp(gmask);
+            if (need_v) {
+                if constexpr (G <= 8) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) dt[i] = reduce_scatter<G>(pd[i], r, gmask);
+                }
+                if (live) {
+                    const float gx = 1.0f - c.fx, gy = 1.0f - c.fy;
+                    const float w[4] = {gx * gy, c.fx * gy, gx * c.fy, c.fx * c.fy};
+                    const float dwx[4] = {-gy, gy, -c.fy, c.fy};
+                    const float dwy[4] = {-gx, -c.fx, gx, c.fx};
+                    float ga = 0.0f, tx = 0.0f, ty = 0.0f;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float di = (c.valid & (1u << i)) ? dt[i] : 0.0f;
+                        ga = fmaf(w[i], di, ga);
+                        tx = fmaf(dwx[i], di, tx);
+                        ty = fmaf(dwy[i], di, ty);
+                    }
+                    if (want_ga) stl(grad_attn, ao + j, ga, p.loc_dt);
+                    if (want_gl) {
+                        stl(grad_loc, lrow + j * sJ, A * tx * (lt.sx[l] * c.kx), p.loc_dt);
+                        stl(grad_loc, lrow + j * sJ + sXY, A * ty * (lt.sy[l] * c.ky), p.loc_dt);
+                    }
+                }
+            }
+        }
+    }
+    // flush: each group adds staged pixels' rows into the global accumulator
+    __syncthreads();
+    for (int l = sp.ls; l < p.N_l; ++l) {
+        const int n = lt.H[l] * lt.W[l];
+        for (int pl = (int)threadIdx.x / G; pl < n; pl += GPB) {
+            const int px = sps[l] + pl;
+#pragma unroll
+            for (int k = 0; k < NCH; ++k)
+                if (k < nk) {
+                    const int ck = ((k * G + r) + (px & sp.rot)) & (p.chunks - 1);
+                    const int cc = sp.rot ? ck : k * G + r;
+                    float v[VEC];
+                    bool any = false;
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e) {
+                        v[e] = acc_s[px * C + cc * VEC + e];
+                        any |= v[e] != 0.0f;
+                    }
+                    if (any) RedIO<VEC>::add(gbh + (lt.start[l] + pl) * sP + k * G * VEC, v, 1.0f);
+                }
+        }
+    }
+}
+
+// Host side (msda_staged_{f32,bf16}.cu): pick the kernel for (G, NCH,
 // padding), size the grid (blocks per (b, h) from the occupancy at `smem`
 // bytes) and launch.
 template <typename T>
 cudaError_t launch_forward_staged(const Params &p, StagePlan sp, const CUtensorMap &tmap, size_t smem, int G, int NCH,
                                   const T *value, const float *loc, const float *attn, T *out,
                                   unsigned int *timeouts, cudaStream_t stream);
+template <typename T>
+cudaError_t launch_backward_staged(const Params &p, StagePlan sp, size_t smem, int G, int NCH, const T *grad_out,
+                                   const T *value, const float *loc, const float *attn, float *gv_acc,
+                                   float *grad_loc, float *grad_attn, cudaStream_t stream);
 
 }  // namespace msda

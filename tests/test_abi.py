@@ -107,8 +107,16 @@ def test_rejections_forward(lib, entry):
 
 
 @no_gpu
-def test_rejections_backward(lib):
+@pytest.mark.parametrize("entry", ["msda_backward", "msda_backward_staged"])
+def test_rejections_backward(lib, entry):
+    """Both backward entry points validate the same way."""
     d = msda.make_desc(DIMS, LEVELS, STARTS)
+
+    def _bwd(lib, desc, flags=(1, 1, 1), ws=None, ws_bytes=0, **ptrs):
+        p = dict(go=FAKE, value=FAKE, loc=FAKE, attn=FAKE, gv=FAKE, gl=FAKE, ga=FAKE)
+        p.update(ptrs)
+        return getattr(lib, entry)(desc.ref(), p["go"], p["value"], p["loc"], p["attn"], *flags, p["gv"], p["gl"],
+                                   p["ga"], ws, ws_bytes, None)
     assert _bwd(lib, d, flags=(0, 0, 0)) == -4
     assert _bwd(lib, d, flags=(2, 0, 0)) == -2
     assert _bwd(lib, d, gv=None) == -1
@@ -203,3 +211,35 @@ def test_staged_levels_rejects_bad_input(lib):
     bad = msda.make_desc(DIMS, LEVELS, (1, 24))
     n = ctypes.c_int(0)
     assert lib.msda_forward_staged_levels(bad.ref(), ctypes.byref(n)) == -5
+
+
+def test_backward_staged_level_choice():
+    """The shared accumulator is binary32 whatever value's dtype (C_h * 4
+    bytes a pixel, 40 KB): level 3 for every workload; none at C_h = 64
+    (73 KB); C_h = 12 (48 B a pixel) keeps level 3 only (level 2 would make it
+    64 KB); not for the scalar path or wide rows."""
+    from scale_deformable_attention_forward_gb300 import inputs as gen
+    W = gen.WORKLOADS
+
+    def lv(w, C_h=None, **over):
+        kw = dict(value_layout=w.value_layout, sampling_locations_layout=w.loc_layout,
+                  align_corners=w.align_corners, padding_mode=w.padding_mode,
+                  value_dtype=msda.DTYPE_BF16 if w.dtype == "bf16" else msda.DTYPE_F32)
+        kw.update(over)
+        dims = (w.B, w.n_queries, w.N_h, C_h or w.C_h, w.N_l, w.N_p, w.L)
+        return msda.backward_staged_levels(msda.make_desc(dims, w.levels, w.level_start_index, **kw))
+
+    for name in ("encoder32", "decoder", "encoder16", "hires16"):
+        assert lv(W[name]) == 3, name
+    w = W["encoder32"]
+    assert lv(w, 64) == w.N_l
+    assert lv(w, 12) == 3
+    assert lv(w, 5) == w.N_l
+    assert lv(w, 96) == w.N_l
+    d = msda.make_desc(DIMS, LEVELS, STARTS)
+    assert lib_staged_rejects(d)
+
+
+def lib_staged_rejects(d):
+    lib = msda.load_library()
+    return lib.msda_backward_staged_levels(d.ref(), None) == -1

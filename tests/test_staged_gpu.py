@@ -159,3 +159,90 @@ def test_staged_kernel_runs_and_never_times_out():
         pytest.skip("the profiler recorded no CUDA kernels here")
     assert any("msda_forward_staged_kernel" in n for n in names), names
     assert msda.staged_timeouts() == 0
+
+
+# ------------------------------------------------------------------ staged backward
+FLAGS_GV = [(True, True, True), (True, False, False), (True, True, False), (True, False, True)]
+
+
+def _bwd_both(w, flags, d=None):
+    import scale_deformable_attention_forward_gb300 as msda
+    d = gen.generate(w) if d is None else d
+    t = to_device(d, w.dtype)
+    args = (t["grad_output"], t["value"], d["spatial_shapes"], d["level_start_index"], t["sampling_locations"],
+            t["attention_weights"])
+    kw = dict(compute_grad_value=flags[0], compute_grad_sampling_locations=flags[1],
+              compute_grad_attention_weights=flags[2], **kw_of(w))
+    direct = [x.clone() if x is not None else None for x in msda.msda_backward(*args, **kw)]
+    staged = msda.msda_backward_staged(*args, **kw)
+    torch.cuda.synchronize()
+    return d, direct, staged
+
+
+def _bwd_check(w, flag_sets=FLAGS_GV, d=None, oracle=True):
+    from parity_util import oracle_backward
+    d = gen.generate(w) if d is None else d
+    for flags in flag_sets:
+        d, direct, staged = _bwd_both(w, flags, d)
+        for name, a, b, f in zip(("grad_value", "grad_sampling_locations", "grad_attention_weights"), staged, direct,
+                                 flags):
+            if not f:
+                assert a is None and b is None
+                continue
+            if name == "grad_value":  # summation order differs: within the backward tolerance of each other
+                assert_close(np64(a), np64(b), RTOL[(w.dtype, "bwd")], f"{w.name} {name} staged vs direct")
+            else:  # the direct kernel's arithmetic
+                assert torch.equal(a, b), f"{w.name} {name} {flags}: staged and direct differ"
+        if oracle:
+            ref = oracle_backward(w, d, flags)
+            for name, a, r, f in zip(("grad_value", "grad_sampling_locations", "grad_attention_weights"), staged,
+                                     ref, flags):
+                if f:
+                    assert_close(np64(a), r, RTOL[(w.dtype, "bwd")], f"{w.name} {name} {flags} staged vs oracle")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("vl,ll,align,pad", [("BLNC", "BQHLP2", False, "zeros"), ("BNLC", "B2QHLP", True, "border"),
+                                             ("BLNC", "B2QHLP", True, "zeros"), ("BNLC", "BQHLP2", False, "border")])
+@pytest.mark.parametrize("levels", [ALL_FIT, COARSE_FIT], ids=["all", "coarse"])
+def test_backward_staged_matrix(dtype, vl, ll, align, pad, levels):
+    import scale_deformable_attention_forward_gb300 as msda
+    w = _small(dtype, vl, ll, align, pad, levels)
+    assert msda.backward_staged_levels(_desc(w)) == (0 if levels is ALL_FIT else 1)
+    _bwd_check(w)
+
+
+@pytest.mark.parametrize("dtype,C_h", [("f32", 4), ("f32", 8), ("f32", 12), ("f32", 16), ("f32", 64), ("bf16", 8),
+                                       ("bf16", 16), ("bf16", 64)])
+def test_backward_staged_lane_shapes(dtype, C_h):
+    """Every staged lane shape, and C_h = 12 (three chunks: no bank rotation,
+    one lane of four past the channels)."""
+    w = _small(dtype, "BLNC", "BQHLP2", False, "zeros", COARSE_FIT, C_h=C_h, N_q=70, N_h=2, seed=440 + C_h)
+    _bwd_check(w, flag_sets=FLAGS_GV[:2])
+
+
+@pytest.mark.parametrize("case", ["scalar", "wide", "no_grad_value"])
+def test_backward_staged_falls_back(case):
+    import scale_deformable_attention_forward_gb300 as msda
+    w = {"scalar": _small("f32", "BLNC", "BQHLP2", False, "zeros", ALL_FIT, C_h=5, N_q=40),
+         "wide": _small("f32", "BLNC", "BQHLP2", False, "zeros", ALL_FIT, C_h=96, N_q=40),
+         "no_grad_value": _small("f32", "BLNC", "BQHLP2", False, "zeros", ALL_FIT, N_q=40)}[case]
+    flags = [(False, True, True)] if case == "no_grad_value" else FLAGS_GV[:1]
+    if case != "no_grad_value":
+        assert msda.backward_staged_levels(_desc(w)) == w.N_l
+    _bwd_check(w, flag_sets=flags)
+
+
+@pytest.mark.parametrize("N_q,B,N_h", [(1, 1, 1), (65, 1, 2), (129, 3, 1)])
+def test_backward_staged_block_tails(N_q, B, N_h):
+    _bwd_check(_small("f32", "BNLC", "B2QHLP", True, "border", ALL_FIT, N_q=N_q, B=B, N_h=N_h, seed=450 + N_q),
+               flag_sets=FLAGS_GV[:1])
+
+
+@pytest.mark.parametrize("name", ["encoder32", "hires16"])
+def test_backward_staged_full_size(name):
+    """Full workloads: the location and attention gradients bit-identical to
+    msda_backward, grad_value within tolerance of it (and of the oracle for
+    the binary32 encoder)."""
+    w = gen.WORKLOADS[name]
+    _bwd_check(w, flag_sets=FLAGS_GV[:1], oracle=name == "encoder32")
