@@ -147,7 +147,8 @@ int msda_forward(const msda_desc *desc, const void *value, const void *sampling_
  * L >= 32; otherwise, and when no level
  * fits, the call runs msda_forward's kernel.  A block whose copy has not
  * completed after a bounded wait gathers every level from global memory and
- * is counted (msda_staged_timeouts). */
+ * is counted (msda_staged_timeouts).  The first call on a device looks up
+ * that counter's device address: make it before any stream capture. */
 int msda_forward_staged(const msda_desc *desc, const void *value, const void *sampling_locations,
                         const void *attention_weights, void *out, cudaStream_t stream);
 

@@ -11,7 +11,13 @@ The functions follow the pages "MS Deformable Attention Kernel API
 Reference" (``msda_forward``) and "MS Deformable Attention Backward Kernel API
 Reference" (``msda_backward``): same argument names, layouts
 (value ``BLNC``/``BNLC``, sampling_locations ``BQHLP2``/``B2QHLP``),
-``align_corners``, ``padding_mode`` and ``compute_grad_*`` flags.
+``align_corners``, ``padding_mode`` and ``compute_grad_*`` flags.  Beside
+them: ``msda_backward_accumulate`` (adds into a persistent float32
+grad_value), ``msda_forward_logits`` / ``msda_backward_logits`` (softmax of
+attention logits inside the kernels), and the staged variants
+``msda_forward_staged`` / ``msda_backward_staged`` (coarse levels held in
+shared memory; same results, measured slower on GB300 than the direct
+kernels the plain calls use).
 """
 from __future__ import annotations
 
@@ -21,6 +27,8 @@ import threading
 from typing import Optional, Sequence, Tuple, Union
 
 __all__ = ["msda_forward", "msda_backward", "msda_backward_workspace_size", "msda_status_string",
+           "msda_backward_accumulate", "msda_forward_logits", "msda_backward_logits", "msda_forward_staged",
+           "msda_backward_staged", "staged_levels", "backward_staged_levels", "staged_timeouts",
            "MSDAError", "library_path", "load_library", "make_desc"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))

@@ -11,6 +11,7 @@
 #include <limits.h>
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
 
 namespace {
@@ -666,6 +667,23 @@ int backward_entry(const msda_desc *desc, const void *grad_output, const void *v
 // Blocks of the staged forward that gave up waiting for their copy.
 __device__ unsigned int g_stage_timeouts = 0;
 
+// The counter's device address on the current device, looked up once per
+// device (null when the lookup fails).
+unsigned int *stage_timeout_counter() {
+    constexpr int kMaxDevices = 64;
+    static std::atomic<unsigned int *> cache[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    unsigned int *c = cache[dev].load(std::memory_order_acquire);
+    if (!c) {
+        void *a = nullptr;
+        if (cudaGetSymbolAddress(&a, g_stage_timeouts) != cudaSuccess) return nullptr;
+        c = static_cast<unsigned int *>(a);
+        cache[dev].store(c, std::memory_order_release);
+    }
+    return c;
+}
+
 int staged_timeouts(unsigned int *count) {
     if (!count) return MSDA_ERR_NULL_POINTER;
     return record_cuda(cudaMemcpyFromSymbol(count, g_stage_timeouts, sizeof(unsigned int)));
@@ -702,8 +720,8 @@ int forward_entry(const msda_desc *desc, const void *value, const void *sampling
     CUtensorMap tm;
     if (staged && !logits && samples > 0 && plan_stage(d, cfg, value, &sp, &smem) &&
         encode_value_map(d, value, &tm)) {
-        unsigned int *timeouts = nullptr;
-        e = cudaGetSymbolAddress((void **)&timeouts, g_stage_timeouts);
+        unsigned int *timeouts = stage_timeout_counter();
+        e = timeouts ? cudaSuccess : cudaErrorInvalidSymbol;
         if (e == cudaSuccess) {
             if (d->value_dtype == MSDA_DTYPE_F32)
                 e = launch_forward_staged<float>(p, sp, tm, smem, cfg.G, cfg.NCH, (const float *)value,

@@ -14,14 +14,16 @@
 // walks its N_l*N_p samples in order; a warp therefore serves 32/G rows at
 // once, rows ordered (b, h, q) so that the rows of a warp and of a block are
 // neighbouring queries of one head (their samples reuse value lines in L1).
-// Inside a group, lane r owns the 16-byte channel chunks r, r+G, r+2G, ...
-// (NCH of them, VEC elements each), so each load instruction of a group reads
-// G*16 contiguous bytes of a corner's channel row.  The G lanes of a group
-// compute the sample's bilinear cell redundantly: that costs fewer
-// instructions than distributing it, and the forward needs no cross-lane
-// communication at all.  The backward reduces its three per-sample dot
-// products over the G lanes with shuffles and scatters grad_value with
-// vector atomics (red.global.add.v4.f32).
+// Inside a group, lane r owns the channel chunks r, r+G, r+2G, ... (NCH of
+// them, VEC elements each), so each load instruction of a group reads one
+// contiguous piece of a corner's channel row.  The samples are taken G at a
+// time: lane r computes sample j0 + r's bilinear cell once and hands it to
+// the group (the forward by shuffles, the backward through swizzled
+// shared-memory records).  The backward sums its per-sample dot products over
+// the G lanes with a transposed butterfly and scatters grad_value with vector
+// atomics (red.global.add.v4.f32), or, for grad_value-only calls on dense
+// problems, through the tile-sorted path further down.  The staged variants
+// (coarse levels in shared memory) are in msda_staged.cuh.
 #pragma once
 
 #include <cuda_runtime.h>

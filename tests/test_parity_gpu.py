@@ -305,3 +305,63 @@ def test_repeatable_sorted(pad):
         assert_close(np64(a[0]), np64(runs[0][0]), 1e-5, "grad_value run to run")
     for g in gvs:
         assert_close(np64(g), np64(runs[0][0]), 1e-5, "tile-sorted grad_value run to run")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_cuda_graph_capture(dtype):
+    """Every call only enqueues work on the caller's stream, so a training
+    step can be captured in a CUDA graph (after one call outside the capture):
+    replays reproduce the eager results -- forward, full backward, the
+    tile-sorted grad_value-only backward, and both staged variants."""
+    import scale_deformable_attention_forward_gb300 as msda
+    w = _dense(_small(dtype, "BLNC", "BQHLP2", False, "zeros", N_q=150, seed=19))
+    d = gen.generate(w)
+    t = to_device(d, w.dtype)
+    kw = dict(value_layout=w.value_layout, sampling_locations_layout=w.loc_layout,
+              align_corners=w.align_corners, padding_mode=w.padding_mode)
+    a = (d["spatial_shapes"], d["level_start_index"], t["sampling_locations"], t["attention_weights"])
+    ws = torch.empty(max(1, msda.msda_backward_workspace_size(t["value"], d["spatial_shapes"], d["level_start_index"],
+                                                              t["sampling_locations"], w.value_layout,
+                                                              w.loc_layout)), dtype=torch.uint8, device="cuda")
+
+    def buffers():
+        return dict(out=torch.empty((w.B, w.n_queries, w.N_h * w.C_h), dtype=t["value"].dtype, device="cuda"),
+                    out_st=torch.empty((w.B, w.n_queries, w.N_h * w.C_h), dtype=t["value"].dtype, device="cuda"),
+                    gv=torch.empty_like(t["value"]), gl=torch.empty_like(t["sampling_locations"]),
+                    ga=torch.empty_like(t["attention_weights"]), gv1=torch.empty_like(t["value"]),
+                    gv_st=torch.empty_like(t["value"]), gl_st=torch.empty_like(t["sampling_locations"]),
+                    ga_st=torch.empty_like(t["attention_weights"]))
+
+    def step(b):
+        msda.msda_forward(t["value"], *a, out=b["out"], **kw)
+        msda.msda_backward(t["grad_output"], t["value"], *a, grad_value=b["gv"], grad_sampling_locations=b["gl"],
+                           grad_attention_weights=b["ga"], workspace=ws, **kw)
+        msda.msda_backward(t["grad_output"], t["value"], *a, compute_grad_sampling_locations=False,
+                           compute_grad_attention_weights=False, grad_value=b["gv1"], workspace=ws, **kw)
+        msda.msda_forward_staged(t["value"], *a, out=b["out_st"], **kw)
+        msda.msda_backward_staged(t["grad_output"], t["value"], *a, grad_value=b["gv_st"],
+                                  grad_sampling_locations=b["gl_st"], grad_attention_weights=b["ga_st"],
+                                  workspace=ws, **kw)
+
+    eager = buffers()
+    step(eager)
+    torch.cuda.synchronize()
+    cap = buffers()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step(cap)  # one call on the capture stream first
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    for v in cap.values():
+        v.zero_()
+    with torch.cuda.graph(g):
+        step(cap)
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    for k in ("out", "out_st", "gl", "ga", "gl_st", "ga_st"):
+        assert torch.equal(cap[k], eager[k]), k
+    for k in ("gv", "gv1", "gv_st"):
+        assert_close(np64(cap[k]), np64(eager[k]), RTOL[(dtype, "bwd")], f"{k} replay")
