@@ -258,6 +258,19 @@ BwdPlan plan_backward(const msda_desc *d, int compute_grad_value, bool allow_sor
     return w;
 }
 
+// Parts a row's samples are split into (log2; see block_rows): more than one
+// only while rows x lanes fill at most half of the GPU's resident threads
+// (2048 a multiprocessor), every part keeps at least one batch of G samples
+// and a row's parts stay within one warp.
+int choose_split(const Params &p, int G, bool allowed) {
+    if (!allowed || p.rows == 0) return 0;
+    const uint64_t capacity = (uint64_t)(p.n_sm > 0 ? p.n_sm : 1) * 2048;
+    const uint64_t lanes = (uint64_t)p.rows * (uint64_t)G;
+    int s = 0;
+    while ((G << (s + 1)) <= 32 && (int64_t)((2 << s) - 1) * G < p.NLP && (lanes << (s + 1)) * 2 <= capacity) ++s;
+    return s;
+}
+
 // Staged-level forward (msda_forward_staged): the coarsest levels, from the
 // last one down, whose pixels of one head fit MSDA_STAGE_BYTES of shared
 // memory, each level's region rounded up to whole TMA boxes.  40 KB keeps
@@ -610,6 +623,7 @@ int backward_entry(const msda_desc *desc, const void *grad_output, const void *v
     p.flags = (fv ? kGradValue : 0) | (fl ? kGradLoc : 0) | (fa ? kGradAttn : 0);
     p.logits = mode.logits ? 1 : 0;
     p.n_sm = samples > 0 ? sm_count() : 0;
+    p.split_log2 = choose_split(p, cfg.G, !mode.logits);  // the logits' gradient needs whole rows
 
     cudaError_t e = cudaSuccess;
     if (fv && !accumulate) e = launch_zero_f32(bb.gv_acc, value_elems, stream);
@@ -714,6 +728,7 @@ int forward_entry(const msda_desc *desc, const void *value, const void *sampling
     Params p = make_params(d, cfg, V);
     p.n_sm = sm_count();
     p.logits = logits ? 1 : 0;
+    p.split_log2 = choose_split(p, cfg.G, true);
     cudaError_t e;
     StagePlan sp;
     size_t smem = 0;

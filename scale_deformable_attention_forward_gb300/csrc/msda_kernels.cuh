@@ -59,6 +59,7 @@ struct Params {
     int flags;      // kGradValue | kGradLoc | kGradAttn (backward)
     int logits;     // 1: `attention_weights` holds logits; A = softmax over the row's N_l*N_p of them
     int loc_dt;     // dtype of locations, weights and their gradients: 0 binary32, 1 bfloat16, 2 binary16
+    int split_log2; // row kernels: each row's samples split over 2^split_log2 groups (see block_rows)
     // value (and grad_value / accumulator) element strides
     int64_t v_sB;
     int v_sH, v_sP;
@@ -334,21 +335,41 @@ template <int G> __device__ __forceinline__ int rec_pos(int g, int s) {
     else return g * G + s;
 }
 
-// Rows of a block: the blocks (as many as fit on the GPU at once) sweep the
-// rows together, GPB consecutive rows per block and step, so at any time the
-// whole GPU works on one window of neighbouring queries: value lines are
-// shared in L2 by the multiprocessors and in L1 by a block's groups.  (Giving
-// each block its own contiguous run of rows measured slower.)
+// Work items of a block: the blocks (as many as fit on the GPU at once) sweep
+// the items together, GPB consecutive items per block and step, so at any
+// time the whole GPU works on one window of neighbouring queries: value lines
+// are shared in L2 by the multiprocessors and in L1 by a block's groups.
+// (Giving each block its own contiguous run of rows measured slower.)  An
+// item is one part of a row: with S = 2^split_log2 parts (chosen > 1 only when
+// the rows alone would leave most of the GPU idle), item t is part t % S of
+// row t / S, and part k takes the row's sample batches k, k + S, k + 2S, ...
+// The S parts of a row are neighbouring groups of one warp, so the forward
+// sums their partial outputs with shuffles; the row's dependent chain of
+// loads is S times shorter.
 struct RowRange {
     uint32_t beg, end, step;
 };
 template <int GPB>
-__device__ __forceinline__ RowRange block_rows(const Params &p) {
+__device__ __forceinline__ RowRange block_rows(const Params &p, int split_log2) {
     RowRange rr;
     rr.beg = blockIdx.x * GPB;
-    rr.end = p.rows;
+    rr.end = p.rows << split_log2;
     rr.step = gridDim.x * GPB;
     return rr;
+}
+
+// Sum a row's S part accumulators over its S groups (lanes G, 2G, ... apart;
+// `lane` is the caller's lane in the warp); every part ends with the total.
+template <int G, int NCH, int VEC>
+__device__ __forceinline__ void sum_parts(float (&acc)[NCH][VEC], int split_log2, int lane) {
+    if (split_log2 == 0) return;
+    const int span = G << split_log2;  // lanes of the row (<= 32)
+    const unsigned pmask = span >= 32 ? 0xffffffffu : (((1u << span) - 1u) << (lane & ~(span - 1)));
+    for (int o = G; o < span; o <<= 1)
+#pragma unroll
+        for (int k = 0; k < NCH; ++k)
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) acc[k][e] += __shfl_xor_sync(pmask, acc[k][e], o);
 }
 
 // Softmax of one row's N_l*N_p attention logits (the attention weights the
@@ -424,7 +445,7 @@ __device__ __forceinline__ FwdCell fwd_cell(const Cell &c, float A, int W, int H
 // binary32 weights (p.loc_dt == 0, p.logits == 0, the common case compiled
 // without the branches), true reads both at run time (with the backward's
 // register budget: the softmax statistics need registers).
-template <typename T, int VEC, int G, int NCH, int PAD, bool GEN>
+template <typename T, int VEC, int G, int NCH, int PAD, bool GEN, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, row_min_blocks(NCH *VEC, !GEN))
 msda_forward_kernel(const __grid_constant__ Params p, const T *__restrict__ value, const float *__restrict__ loc,
                     const float *__restrict__ attn, T *__restrict__ out) {
@@ -439,9 +460,13 @@ msda_forward_kernel(const __grid_constant__ Params p, const T *__restrict__ valu
     int nk = 0;  // chunks this lane owns: k*G + r < chunks
 #pragma unroll
     for (int k = 0; k < NCH; ++k) nk += (k * G + r < p.chunks);
-    const RowRange rr = block_rows<GPB>(p);
+    const int slog = SPLIT ? p.split_log2 : 0;  // (SPLIT = false: the whole-row kernel, no split code)
+    const RowRange rr = block_rows<GPB>(p, slog);
+    const int jstep = G << slog;
 
-    for (uint32_t row = rr.beg + threadIdx.x / G; row < rr.end; row += rr.step) {
+    for (uint32_t item = rr.beg + threadIdx.x / G; item < rr.end; item += rr.step) {
+        const uint32_t row = item >> slog;
+        const int part = (int)(item & ((1u << slog) - 1u));
         const Row rw = decode_row(p, row);
         const T *vbh = value + rw.b * p.v_sB + (int64_t)rw.h * p.v_sH + r * VEC;
         const int64_t lo = rw.b * p.l_sB + (int64_t)((rw.q * (uint32_t)p.N_h + rw.h) * (uint32_t)NLP) * sJ;
@@ -456,7 +481,7 @@ msda_forward_kernel(const __grid_constant__ Params p, const T *__restrict__ valu
 #pragma unroll
             for (int e = 0; e < VEC; ++e) acc[k][e] = 0.0f;
 
-        for (int j0 = 0; j0 < NLP; j0 += G) {
+        for (int j0 = part * G; j0 < NLP; j0 += jstep) {
             // owner phase: this lane's sample (past the last sample: weight 0 at offset 0)
             FwdCell mine = {0, 0, 0.0f, 0.0f, 0.0f, 0.0f};
             const int j = j0 + r;
@@ -515,10 +540,13 @@ msda_forward_kernel(const __grid_constant__ Params p, const T *__restrict__ valu
                 }
             }
         }
+        if constexpr (SPLIT) sum_parts<G, NCH, VEC>(acc, slog, lane);
         T *dst = out + (int64_t)rw.bqh * p.C_h + r * VEC;
+        if (part == 0) {
 #pragma unroll
-        for (int k = 0; k < NCH; ++k)
-            if (k < nk) VecIO<T, VEC>::store(dst + k * G * VEC, acc[k]);
+            for (int k = 0; k < NCH; ++k)
+                if (k < nk) VecIO<T, VEC>::store(dst + k * G * VEC, acc[k]);
+        }
     }
 }
 
@@ -576,7 +604,7 @@ __device__ __forceinline__ int bucket_of(const Cell &c, int bst, int BX, int *ce
 // FL: kGradValue|kGradLoc|kGradAttn or kGradValue (exactly these outputs),
 // kGradLoc|kGradAttn (no grad_value; the two others as p.flags says), or -1
 // (everything from p.flags at run time).  PAD as in the forward.
-template <typename T, int VEC, int G, int NCH, int PAD, int FL>
+template <typename T, int VEC, int G, int NCH, int PAD, int FL, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, row_min_blocks(NCH *VEC, false))
 msda_backward_kernel(const __grid_constant__ Params p, const T *__restrict__ grad_out, const T *__restrict__ value,
                      const float *__restrict__ loc, const float *__restrict__ attn, float *__restrict__ gv_acc,
@@ -603,9 +631,14 @@ msda_backward_kernel(const __grid_constant__ Params p, const T *__restrict__ gra
     int nk = 0;  // chunks this lane owns: k*G + r < chunks
 #pragma unroll
     for (int k = 0; k < NCH; ++k) nk += (k * G + r < p.chunks);
-    const RowRange rr = block_rows<GPB>(p);
+    // split only without logits (the rewrite below needs whole rows); SPLIT = false: no split code
+    const int slog = SPLIT ? p.split_log2 : 0;
+    const RowRange rr = block_rows<GPB>(p, slog);
+    const int jstep = G << slog;
 
-    for (uint32_t row = rr.beg + threadIdx.x / G; row < rr.end; row += rr.step) {
+    for (uint32_t item = rr.beg + threadIdx.x / G; item < rr.end; item += rr.step) {
+        const uint32_t row = item >> slog;
+        const int part = (int)(item & ((1u << slog) - 1u));
         const Row rw = decode_row(p, row);
         const int64_t bhoff = rw.b * p.v_sB + (int64_t)rw.h * p.v_sH;
         const T *vbh = value + bhoff + r * VEC;
@@ -630,7 +663,7 @@ msda_backward_kernel(const __grid_constant__ Params p, const T *__restrict__ gra
             }
         }
 
-        for (int j0 = 0; j0 < NLP; j0 += G) {
+        for (int j0 = part * G; j0 < NLP; j0 += jstep) {
             // owner phase: this lane's sample
             const int j = j0 + r;
             const bool live = j < NLP;

@@ -26,20 +26,31 @@ int resident_blocks(K kernel, int threads, size_t smem) {
 template <typename K>
 unsigned row_grid(K kernel, int G, const Params &p) {
     const unsigned gpb = kThreads / G;  // rows a block works on at once
-    uint64_t blocks = ((uint64_t)p.rows + gpb - 1) / gpb;
+    uint64_t blocks = (((uint64_t)p.rows << p.split_log2) + gpb - 1) / gpb;  // work items: rows x parts
     const int per_sm = resident_blocks(kernel, kThreads, 0);
     if (per_sm > 0 && p.n_sm > 0 && (uint64_t)per_sm * p.n_sm < blocks) blocks = (uint64_t)per_sm * p.n_sm;
     if (blocks < 1) blocks = 1;
     return (unsigned)blocks;
 }
 
-template <typename T, int V, int GG, int NN, int PAD, bool GEN>
+// SPLIT: the kernel with the row split (p.split_log2 > 0, small problems);
+// the others run whole rows (their launches see split_log2 = 0).
+template <typename T, int V, int GG, int NN, int PAD, bool GEN, bool SPLIT>
 cudaError_t fwd_launch(const Params &p, const T *value, const float *loc, const float *attn, T *out,
                        cudaStream_t stream) {
-    auto kernel = msda_forward_kernel<T, V, GG, NN, PAD, GEN>;
-    const unsigned blocks = row_grid(kernel, GG, p);
-    kernel<<<blocks, kThreads, 0, stream>>>(p, value, loc, attn, out);
+    Params q = p;
+    if (!SPLIT) q.split_log2 = 0;
+    auto kernel = msda_forward_kernel<T, V, GG, NN, PAD, GEN, SPLIT>;
+    const unsigned blocks = row_grid(kernel, GG, q);
+    kernel<<<blocks, kThreads, 0, stream>>>(q, value, loc, attn, out);
     return cudaGetLastError();
+}
+
+template <typename T, int V, int GG, int NN, int PAD, bool GEN>
+cudaError_t fwd_split(const Params &p, const T *value, const float *loc, const float *attn, T *out,
+                      cudaStream_t stream) {
+    return p.split_log2 > 0 ? fwd_launch<T, V, GG, NN, PAD, GEN, true>(p, value, loc, attn, out, stream)
+                            : fwd_launch<T, V, GG, NN, PAD, GEN, false>(p, value, loc, attn, out, stream);
 }
 
 template <typename T, int V, int GG, int NN>
@@ -48,12 +59,12 @@ cudaError_t fwd_shape(const Params &p, const T *value, const float *loc, const f
     if constexpr (V > 1 && specialised_shape(GG, NN)) {
         const bool gen = p.loc_dt != 0 || p.logits != 0;
         if (p.padding == 0)
-            return gen ? fwd_launch<T, V, GG, NN, 0, true>(p, value, loc, attn, out, stream)
-                       : fwd_launch<T, V, GG, NN, 0, false>(p, value, loc, attn, out, stream);
-        return gen ? fwd_launch<T, V, GG, NN, 1, true>(p, value, loc, attn, out, stream)
-                   : fwd_launch<T, V, GG, NN, 1, false>(p, value, loc, attn, out, stream);
+            return gen ? fwd_split<T, V, GG, NN, 0, true>(p, value, loc, attn, out, stream)
+                       : fwd_split<T, V, GG, NN, 0, false>(p, value, loc, attn, out, stream);
+        return gen ? fwd_split<T, V, GG, NN, 1, true>(p, value, loc, attn, out, stream)
+                   : fwd_split<T, V, GG, NN, 1, false>(p, value, loc, attn, out, stream);
     } else {
-        return fwd_launch<T, V, GG, NN, -1, true>(p, value, loc, attn, out, stream);
+        return fwd_launch<T, V, GG, NN, -1, true, false>(p, value, loc, attn, out, stream);
     }
 }
 
@@ -72,12 +83,14 @@ cudaError_t launch_forward_path(const Params &p, int G, int NCH, const T *value,
     return cudaErrorInvalidConfiguration;
 }
 
-template <typename T, int V, int GG, int NN, int PAD, int FL>
+template <typename T, int V, int GG, int NN, int PAD, int FL, bool SPLIT>
 cudaError_t bwd_launch(const Params &p, const T *grad_out, const T *value, const float *loc, const float *attn,
                        const BwdBuffers &bb, cudaStream_t stream) {
-    auto kernel = msda_backward_kernel<T, V, GG, NN, PAD, FL>;
-    const unsigned blocks = row_grid(kernel, GG, p);
-    kernel<<<blocks, kThreads, 0, stream>>>(p, grad_out, value, loc, attn, bb.gv_acc, bb.grad_loc, bb.grad_attn);
+    Params q = p;
+    if (!SPLIT) q.split_log2 = 0;
+    auto kernel = msda_backward_kernel<T, V, GG, NN, PAD, FL, SPLIT>;
+    const unsigned blocks = row_grid(kernel, GG, q);
+    kernel<<<blocks, kThreads, 0, stream>>>(q, grad_out, value, loc, attn, bb.gv_acc, bb.grad_loc, bb.grad_attn);
     return cudaGetLastError();
 }
 
@@ -87,15 +100,22 @@ template <typename T, int V, int GG, int NN, int PAD>
 cudaError_t bwd_flags(const Params &p, const T *grad_out, const T *value, const float *loc, const float *attn,
                       const BwdBuffers &bb, cudaStream_t stream) {
     constexpr int ALL = kGradValue | kGradLoc | kGradAttn;
-#define MSDA_BWD(FL) return bwd_launch<T, V, GG, NN, PAD, FL>(p, grad_out, value, loc, attn, bb, stream)
-    if constexpr (PAD < 0 || !specialised_shape(GG, NN)) {
-        MSDA_BWD(-1);
-    } else {
-        if (!(p.flags & kGradValue)) MSDA_BWD(kGradLoc | kGradAttn);
-        if (p.flags == ALL) MSDA_BWD(ALL);
-        if (p.flags == kGradValue) MSDA_BWD(kGradValue);
-        MSDA_BWD(-1);
+#define MSDA_BWD(FL, SPLIT) return bwd_launch<T, V, GG, NN, PAD, FL, SPLIT>(p, grad_out, value, loc, attn, bb, stream)
+#define MSDA_BWD_S(FL)            \
+    {                             \
+        if (p.split_log2 > 0)     \
+            MSDA_BWD(FL, true);   \
+        MSDA_BWD(FL, false);      \
     }
+    if constexpr (PAD < 0 || !specialised_shape(GG, NN)) {
+        MSDA_BWD(-1, false);
+    } else {
+        if (!(p.flags & kGradValue)) MSDA_BWD_S(kGradLoc | kGradAttn);
+        if (p.flags == ALL) MSDA_BWD_S(ALL);
+        if (p.flags == kGradValue) MSDA_BWD_S(kGradValue);
+        MSDA_BWD(-1, false);
+    }
+#undef MSDA_BWD_S
 #undef MSDA_BWD
 }
 

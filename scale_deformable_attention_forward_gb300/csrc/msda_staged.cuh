@@ -140,7 +140,11 @@ msda_forward_staged_kernel(const __grid_constant__ Params p, const __grid_consta
     const T *vbh = value + b * p.v_sB + (int64_t)h * p.v_sH + r * VEC;
     const uint32_t sbr = sbase + (uint32_t)(r * VEC * (int)sizeof(T));  // this lane's channels of shared pixel 0
 
-    for (int q = q0 + (int)threadIdx.x / G; q < q1; q += GPB) {
+    // items as in the direct kernel: part `part` of query q takes its batches part, part + S, ...
+    const int jstep = G << p.split_log2;
+    for (int item = (q0 << p.split_log2) + (int)threadIdx.x / G; item < (q1 << p.split_log2); item += GPB) {
+        const int q = item >> p.split_log2;
+        const int part = item & ((1 << p.split_log2) - 1);
         const uint32_t bqh = (b * (uint32_t)p.N_q + (uint32_t)q) * (uint32_t)p.N_h + h;
         const int64_t lo = b * p.l_sB + (int64_t)(((uint32_t)q * (uint32_t)p.N_h + h) * (uint32_t)NLP) * sJ;
         const int64_t ao = (int64_t)bqh * NLP;
@@ -150,7 +154,7 @@ msda_forward_staged_kernel(const __grid_constant__ Params p, const __grid_consta
 #pragma unroll
             for (int e = 0; e < VEC; ++e) acc[k][e] = 0.0f;
 
-        for (int j0 = 0; j0 < NLP; j0 += G) {
+        for (int j0 = part * G; j0 < NLP; j0 += jstep) {
             // owner phase: staged samples get offsets into shared memory (pixel stride C_h)
             FwdCell mine = {0, 0, 0.0f, 0.0f, 0.0f, 0.0f};
             const int j = j0 + r;
@@ -220,10 +224,13 @@ msda_forward_staged_kernel(const __grid_constant__ Params p, const __grid_consta
                 }
             }
         }
+        sum_parts<G, NCH, VEC>(acc, p.split_log2, lane);
         T *dst = out + (int64_t)bqh * C + r * VEC;
+        if (part == 0) {
 #pragma unroll
-        for (int k = 0; k < NCH; ++k)
-            if (k < nk) VecIO<T, VEC>::store(dst + k * G * VEC, acc[k]);
+            for (int k = 0; k < NCH; ++k)
+                if (k < nk) VecIO<T, VEC>::store(dst + k * G * VEC, acc[k]);
+        }
     }
     // a copy that had not landed must not write into shared memory the next block owns
     if (staging && !ok) stage_wait(bar, 0);
