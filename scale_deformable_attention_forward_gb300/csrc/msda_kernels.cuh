@@ -401,7 +401,8 @@ __device__ __forceinline__ float2 row_softmax_stats(const float *attn, int64_t a
 // lane the forward 4 (64 registers a thread: more warps to hide the gather
 // latency) and the backward 3 (85 registers: its per-sample partials and
 // reduction need them); for two chunks the forward 3 and the backward 2; 2
-// (128 registers) for the wide-row kernels.
+// (128 registers) for the wide-row kernels (one block per SM for the widest
+// backward rows removes their spill but measured slower).
 __host__ __device__ constexpr int row_min_blocks(int elems, bool fwd) {
     return elems <= 4 ? (fwd ? MSDA_FWD_MIN_BLOCKS : MSDA_BWD_MIN_BLOCKS) : (elems <= 8 && fwd) ? 3 : 2;
 }
@@ -499,6 +500,38 @@ msda_forward_kernel(const __grid_constant__ Params p, const T *__restrict__ valu
             constexpr int S2 = (G >= 2 && NCH * VEC <= 4) ? 2 : 1;  // two samples in flight for one chunk a lane
 #pragma unroll
             for (int s = 0; s < G; s += S2) {
+                if constexpr (NCH > 4) {  // wide rows: the same arithmetic, two chunks' corners at a time
+                    if (s < ns) {
+                        const int src = base + s;
+                        const int o0 = __shfl_sync(gmask, mine.o0, src);
+                        const int o1 = __shfl_sync(gmask, mine.o1, src);
+                        const float ax0 = __shfl_sync(gmask, mine.ax0, src);
+                        const float ax1 = __shfl_sync(gmask, mine.ax1, src);
+                        const float ay0 = __shfl_sync(gmask, mine.ay0, src);
+                        const float ay1 = __shfl_sync(gmask, mine.ay1, src);
+                        const int dx = (int)((unsigned)o0 >> 31) * sP;
+                        const int o[4] = {o0 & 0x7fffffff, (o0 & 0x7fffffff) + dx, o1, o1 + dx};
+                        const float w[4] = {ay0 * ax0, ay0 * ax1, ay1 * ax0, ay1 * ax1};
+#pragma unroll
+                        for (int k0 = 0; k0 < NCH; k0 += 2) {
+                            float x[4][2][VEC];
+#pragma unroll
+                            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                                for (int kk = 0; kk < 2; ++kk)
+                                    if (k0 + kk < nk) VecIO<T, VEC>::load(vbh + o[i] + (k0 + kk) * G * VEC, x[i][kk]);
+#pragma unroll
+                            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                                for (int kk = 0; kk < 2; ++kk)
+                                    if (k0 + kk < nk)
+#pragma unroll
+                                        for (int e = 0; e < VEC; ++e)
+                                            acc[k0 + kk][e] = fmaf(w[i], x[i][kk][e], acc[k0 + kk][e]);
+                        }
+                    }
+                    continue;
+                }
                 if (s < ns) {
                     int o[S2][4];
                     float w[S2][4];
@@ -699,19 +732,24 @@ msda_backward_kernel(const __grid_constant__ Params p, const T *__restrict__ gra
                     const int4 o4 = wo[q];
                     const int oo[4] = {o4.x, o4.y, o4.z, o4.w};
                     if (need_v) {
-                        float x[4][NCH][VEC];
+                        // (wide rows: two chunks' corners at a time; each d_i still sums chunk by chunk)
+                        constexpr int KB = NCH > 2 ? 2 : NCH;
 #pragma unroll
-                        for (int i = 0; i < 4; ++i)
+                        for (int k0 = 0; k0 < NCH; k0 += KB) {
+                            float x[4][KB][VEC];
 #pragma unroll
-                            for (int k = 0; k < NCH; ++k)
-                                if (k < nk) VecIO<T, VEC>::load(vbh + oo[i] + k * G * VEC, x[i][k]);
+                            for (int i = 0; i < 4; ++i)
 #pragma unroll
-                        for (int i = 0; i < 4; ++i)
+                                for (int kk = 0; kk < KB; ++kk)
+                                    if (k0 + kk < nk) VecIO<T, VEC>::load(vbh + oo[i] + (k0 + kk) * G * VEC, x[i][kk]);
 #pragma unroll
-                            for (int k = 0; k < NCH; ++k)
-                                if (k < nk)
+                            for (int i = 0; i < 4; ++i)
 #pragma unroll
-                                    for (int e = 0; e < VEC; ++e) d[i] = fmaf(g[k][e], x[i][k][e], d[i]);
+                                for (int kk = 0; kk < KB; ++kk)
+                                    if (k0 + kk < nk)
+#pragma unroll
+                                        for (int e = 0; e < VEC; ++e) d[i] = fmaf(g[k0 + kk][e], x[i][kk][e], d[i]);
+                        }
                     }
                     if (scatter) {
                         const float4 w4 = ww[q];
