@@ -412,12 +412,13 @@ __host__ __device__ constexpr int row_min_blocks(int elems, bool fwd) {
 // of the top-left corner read, with bit 31 set when the right-hand corners
 // read the next pixel to the right (clear when both columns clamp onto the
 // same pixel; offsets are below 2^31), o1 the offset of the bottom-left
-// corner read, and ax0 = A(1-fx), ax1 = A fx, ay0 = 1-fy, ay1 = fy the
-// separable weight factors, each 0 when its column or row lies outside the
-// map ("zeros"): corner (i, k) gets ay_i * ax_k.
+// corner read, and w the four corner weights ay_i * ax_k with ax0 = A(1-fx),
+// ax1 = A fx, ay0 = 1-fy, ay1 = fy, a factor 0 when its column or row lies
+// outside the map ("zeros").  The owner forms the products once, so the
+// group's lanes do not each repeat them.
 struct FwdCell {
     int o0, o1;
-    float ax0, ax1, ay0, ay1;
+    float w00, w01, w10, w11;
 };
 
 __device__ __forceinline__ FwdCell fwd_cell(const Cell &c, float A, int W, int H, int start, int sP) {
@@ -427,10 +428,14 @@ __device__ __forceinline__ FwdCell fwd_cell(const Cell &c, float A, int W, int H
     f.o0 = (int)((unsigned)((start + ya * W + xa) * sP) | ((unsigned)(xb - xa) << 31));
     f.o1 = (start + yb * W + xa) * sP;
     const float A1 = A * c.fx;
-    f.ax0 = (c.valid & 5u) ? A - A1 : 0.0f;  // column x0 lies in the map
-    f.ax1 = (c.valid & 10u) ? A1 : 0.0f;     // column x0 + 1
-    f.ay0 = (c.valid & 3u) ? 1.0f - c.fy : 0.0f;
-    f.ay1 = (c.valid & 12u) ? c.fy : 0.0f;
+    const float ax0 = (c.valid & 5u) ? A - A1 : 0.0f;  // column x0 lies in the map
+    const float ax1 = (c.valid & 10u) ? A1 : 0.0f;     // column x0 + 1
+    const float ay0 = (c.valid & 3u) ? 1.0f - c.fy : 0.0f;
+    const float ay1 = (c.valid & 12u) ? c.fy : 0.0f;
+    f.w00 = ay0 * ax0;
+    f.w01 = ay0 * ax1;
+    f.w10 = ay1 * ax0;
+    f.w11 = ay1 * ax1;
     return f;
 }
 
@@ -505,13 +510,10 @@ msda_forward_kernel(const __grid_constant__ Params p, const T *__restrict__ valu
                         const int src = base + s;
                         const int o0 = __shfl_sync(gmask, mine.o0, src);
                         const int o1 = __shfl_sync(gmask, mine.o1, src);
-                        const float ax0 = __shfl_sync(gmask, mine.ax0, src);
-                        const float ax1 = __shfl_sync(gmask, mine.ax1, src);
-                        const float ay0 = __shfl_sync(gmask, mine.ay0, src);
-                        const float ay1 = __shfl_sync(gmask, mine.ay1, src);
+                        const float w[4] = {__shfl_sync(gmask, mine.w00, src), __shfl_sync(gmask, mine.w01, src),
+                                            __shfl_sync(gmask, mine.w10, src), __shfl_sync(gmask, mine.w11, src)};
                         const int dx = (int)((unsigned)o0 >> 31) * sP;
                         const int o[4] = {o0 & 0x7fffffff, (o0 & 0x7fffffff) + dx, o1, o1 + dx};
-                        const float w[4] = {ay0 * ax0, ay0 * ax1, ay1 * ax0, ay1 * ax1};
 #pragma unroll
                         for (int k0 = 0; k0 < NCH; k0 += 2) {
                             float x[4][2][VEC];
@@ -541,19 +543,15 @@ msda_forward_kernel(const __grid_constant__ Params p, const T *__restrict__ valu
                         const int src = base + s + h2;
                         const int o0 = __shfl_sync(gmask, mine.o0, src);
                         const int o1 = __shfl_sync(gmask, mine.o1, src);
-                        const float ax0 = __shfl_sync(gmask, mine.ax0, src);
-                        const float ax1 = __shfl_sync(gmask, mine.ax1, src);
-                        const float ay0 = __shfl_sync(gmask, mine.ay0, src);
-                        const float ay1 = __shfl_sync(gmask, mine.ay1, src);
+                        w[h2][0] = __shfl_sync(gmask, mine.w00, src);
+                        w[h2][1] = __shfl_sync(gmask, mine.w01, src);
+                        w[h2][2] = __shfl_sync(gmask, mine.w10, src);
+                        w[h2][3] = __shfl_sync(gmask, mine.w11, src);
                         const int dx = (int)((unsigned)o0 >> 31) * sP;
                         o[h2][0] = o0 & 0x7fffffff;
                         o[h2][1] = (o0 & 0x7fffffff) + dx;
                         o[h2][2] = o1;
                         o[h2][3] = o1 + dx;
-                        w[h2][0] = ay0 * ax0;
-                        w[h2][1] = ay0 * ax1;
-                        w[h2][2] = ay1 * ax0;
-                        w[h2][3] = ay1 * ax1;
 #pragma unroll
                         for (int i = 0; i < 4; ++i)
 #pragma unroll

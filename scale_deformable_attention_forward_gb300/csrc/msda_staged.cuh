@@ -179,10 +179,10 @@ msda_forward_staged_kernel(const __grid_constant__ Params p, const __grid_consta
                         const int src = base + s + h2;
                         const int o0 = __shfl_sync(gmask, mine.o0, src);
                         const int o1 = __shfl_sync(gmask, mine.o1, src);
-                        const float ax0 = __shfl_sync(gmask, mine.ax0, src);
-                        const float ax1 = __shfl_sync(gmask, mine.ax1, src);
-                        const float ay0 = __shfl_sync(gmask, mine.ay0, src);
-                        const float ay1 = __shfl_sync(gmask, mine.ay1, src);
+                        w[h2][0] = __shfl_sync(gmask, mine.w00, src);
+                        w[h2][1] = __shfl_sync(gmask, mine.w01, src);
+                        w[h2][2] = __shfl_sync(gmask, mine.w10, src);
+                        w[h2][3] = __shfl_sync(gmask, mine.w11, src);
                         // the same for every lane of the warp; a sample past the row's last
                         // (weight 0, offset 0) reads global memory, as in the direct kernel
                         const bool st = j0 + s + h2 >= lsj && j0 + s + h2 < NLP;
@@ -191,10 +191,6 @@ msda_forward_staged_kernel(const __grid_constant__ Params p, const __grid_consta
                         o[h2][1] = (o0 & 0x7fffffff) + dx;
                         o[h2][2] = o1;
                         o[h2][3] = o1 + dx;
-                        w[h2][0] = ay0 * ax0;
-                        w[h2][1] = ay0 * ax1;
-                        w[h2][2] = ay1 * ax0;
-                        w[h2][3] = ay1 * ax1;
                         if (st) {
 #pragma unroll
                             for (int i = 0; i < 4; ++i)
