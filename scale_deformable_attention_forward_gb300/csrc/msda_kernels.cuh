@@ -18,8 +18,8 @@
 // them, VEC elements each), so each load instruction of a group reads one
 // contiguous piece of a corner's channel row.  The samples are taken G at a
 // time: lane r computes sample j0 + r's bilinear cell once and hands it to
-// the group (the forward by shuffles, the backward through swizzled
-// shared-memory records).  The backward sums its per-sample dot products over
+// the group through swizzled shared-memory records (wide forward rows: by
+// shuffles).  The backward sums its per-sample dot products over
 // the G lanes with a transposed butterfly and scatters grad_value with vector
 // atomics (red.global.add.v4.f32), or, for grad_value-only calls on dense
 // problems, through the tile-sorted path further down.  The staged variants
@@ -397,6 +397,9 @@ __device__ __forceinline__ float2 row_softmax_stats(const float *attn, int64_t a
 #ifndef MSDA_BWD_MIN_BLOCKS
 #define MSDA_BWD_MIN_BLOCKS 3
 #endif
+#ifndef MSDA_FWD_MIN_BLOCKS_F32
+#define MSDA_FWD_MIN_BLOCKS_F32 3
+#endif
 // Blocks per SM the row kernels are compiled for: for one 4-element chunk a
 // lane the forward 4 (64 registers a thread: more warps to hide the gather
 // latency) and the backward 3 (85 registers: its per-sample partials and
@@ -443,25 +446,36 @@ __device__ __forceinline__ FwdCell fwd_cell(const Cell &c, float A, int W, int H
 // consecutive rows of its run, so the rows in flight on a multiprocessor are
 // neighbouring queries of one head and reuse value lines in L1.  The row's
 // samples are taken G at a time: lane r loads sample j0 + r's location and
-// weight (coalesced) and computes its bilinear cell once; the group then
-// walks the G samples, receiving each cell from its owner by shuffles, and
-// loads every corner's channel row with one instruction per channel chunk
-// (lane r owns chunks r, r+G, ...), two samples' corners in flight.
+// weight (coalesced), computes its bilinear cell once and publishes it as a
+// record (four corner offsets, four weights) in shared memory, at the
+// swizzled position the backward uses; the group then walks the G samples,
+// reading each record (two 16-byte loads; rows of more than four chunks a
+// lane take the cell by shuffles instead), and loads every corner's channel
+// row with one instruction per channel chunk (lane r owns chunks r, r+G, ...),
+// two samples' corners in flight.  Binary32 rows of one chunk a lane run at
+// three blocks per SM (80 registers), bfloat16 at four: each measured best.
 // PAD: 0 zeros, 1 border, -1 read p.padding at run time.  GEN: false for
 // binary32 weights (p.loc_dt == 0, p.logits == 0, the common case compiled
 // without the branches), true reads both at run time (with the backward's
 // register budget: the softmax statistics need registers).
 template <typename T, int VEC, int G, int NCH, int PAD, bool GEN, bool SPLIT>
-__global__ void __launch_bounds__(kThreads, row_min_blocks(NCH *VEC, !GEN))
+__global__ void __launch_bounds__(kThreads, (sizeof(T) == 4 && !GEN && NCH * VEC <= 4) ? MSDA_FWD_MIN_BLOCKS_F32
+                                                                                     : row_min_blocks(NCH *VEC, !GEN))
 msda_forward_kernel(const __grid_constant__ Params p, const T *__restrict__ value, const float *__restrict__ loc,
                     const float *__restrict__ attn, T *__restrict__ out) {
     __shared__ LevelTables lt;
+    constexpr bool REC = NCH <= 4;  // cell records in shared memory (wide rows: shuffles)
+    __shared__ int4 rec_o[REC ? kThreads : 1];
+    __shared__ float4 rec_w[REC ? kThreads : 1];
     load_level_tables(p, lt);
     constexpr int GPB = kThreads / G;  // rows in flight per block
     const int lane = threadIdx.x & 31;
     const int r = lane & (G - 1);
     const int base = lane & ~(G - 1);
     const unsigned gmask = G == 32 ? 0xffffffffu : (((1u << G) - 1u) << base);
+    int4 *wo = rec_o + (REC ? (threadIdx.x & ~31) : 0);
+    float4 *ww = rec_w + (REC ? (threadIdx.x & ~31) : 0);
+    const int mypos = rec_pos<G>(lane / G, r);
     const int sP = p.v_sP, sJ = p.l_sJ, sXY = p.l_sXY, NLP = p.NLP;
     int nk = 0;  // chunks this lane owns: k*G + r < chunks
 #pragma unroll
@@ -498,8 +512,18 @@ msda_forward_kernel(const __grid_constant__ Params p, const T *__restrict__ valu
                 const int l = (int)p.div_p.div((uint32_t)j);
                 const int W = lt.W[l], H = lt.H[l];
                 const Cell c = make_cell<PAD>(u, v, lt.sx[l], lt.sy[l], p.off, W, H, p.padding);
-                mine = fwd_cell(c, A, W, H, lt.start[l], sP);
+                if constexpr (REC) {
+                    const Corners cr = corners_of(c, A, W, H, lt.start[l], sP);
+                    wo[mypos] = make_int4(cr.o[0], cr.o[1], cr.o[2], cr.o[3]);
+                    ww[mypos] = make_float4(cr.w[0], cr.w[1], cr.w[2], cr.w[3]);
+                } else {
+                    mine = fwd_cell(c, A, W, H, lt.start[l], sP);
+                }
+            } else if constexpr (REC) {
+                wo[mypos] = make_int4(0, 0, 0, 0);
+                ww[mypos] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
             }
+            if constexpr (REC) __syncwarp(gmask);
             // consume phase: the group's samples in order, corners of two in flight
             const int ns = min(G, NLP - j0);
             constexpr int S2 = (G >= 2 && NCH * VEC <= 4) ? 2 : 1;  // two samples in flight for one chunk a lane
@@ -540,18 +564,18 @@ msda_forward_kernel(const __grid_constant__ Params p, const T *__restrict__ valu
                     float x[S2][4][NCH][VEC];
 #pragma unroll
                     for (int h2 = 0; h2 < S2; ++h2) {
-                        const int src = base + s + h2;
-                        const int o0 = __shfl_sync(gmask, mine.o0, src);
-                        const int o1 = __shfl_sync(gmask, mine.o1, src);
-                        w[h2][0] = __shfl_sync(gmask, mine.w00, src);
-                        w[h2][1] = __shfl_sync(gmask, mine.w01, src);
-                        w[h2][2] = __shfl_sync(gmask, mine.w10, src);
-                        w[h2][3] = __shfl_sync(gmask, mine.w11, src);
-                        const int dx = (int)((unsigned)o0 >> 31) * sP;
-                        o[h2][0] = o0 & 0x7fffffff;
-                        o[h2][1] = (o0 & 0x7fffffff) + dx;
-                        o[h2][2] = o1;
-                        o[h2][3] = o1 + dx;
+                        static_assert(REC || NCH > 4, "up to four chunks a lane: the record exchange");
+                        const int q = rec_pos<G>(lane / G, s + h2);
+                        const int4 o4 = wo[q];
+                        const float4 w4 = ww[q];
+                        o[h2][0] = o4.x;
+                        o[h2][1] = o4.y;
+                        o[h2][2] = o4.z;
+                        o[h2][3] = o4.w;
+                        w[h2][0] = w4.x;
+                        w[h2][1] = w4.y;
+                        w[h2][2] = w4.z;
+                        w[h2][3] = w4.w;
 #pragma unroll
                         for (int i = 0; i < 4; ++i)
 #pragma unroll
@@ -570,6 +594,7 @@ msda_forward_kernel(const __grid_constant__ Params p, const T *__restrict__ valu
                                         acc[k][e] = fmaf(w[h2][i], x[h2][i][k][e], acc[k][e]);
                 }
             }
+            if constexpr (REC) __syncwarp(gmask);  // records are rewritten by the next batch
         }
         if constexpr (SPLIT) sum_parts<G, NCH, VEC>(acc, slog, lane);
         T *dst = out + (int64_t)rw.bqh * p.C_h + r * VEC;
