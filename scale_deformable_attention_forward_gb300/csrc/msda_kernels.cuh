@@ -410,8 +410,10 @@ __host__ __device__ constexpr int row_min_blocks(int elems, bool fwd) {
     return elems <= 4 ? (fwd ? MSDA_FWD_MIN_BLOCKS : MSDA_BWD_MIN_BLOCKS) : (elems <= 8 && fwd) ? 3 : 2;
 }
 
-// One sample's cell in the form the lanes of a group exchange (six 32-bit
-// shuffles): o0 is the element offset (relative to the (b, h) slice of value)
+// One sample's cell in the form the lanes of a group exchange by six 32-bit
+// shuffles (rows wider than four chunks a lane, and the staged forward; the
+// others use the shared-memory records of Corners): o0 is the element offset
+// (relative to the (b, h) slice of value)
 // of the top-left corner read, with bit 31 set when the right-hand corners
 // read the next pixel to the right (clear when both columns clamp onto the
 // same pixel; offsets are below 2^31), o1 the offset of the bottom-left
