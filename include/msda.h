@@ -103,9 +103,11 @@ enum msda_status {
 /* Problem descriptor.  Dimensions follow the pages' Dimensions list:
  *   B batch, N_q queries, N_h heads, C_h channels per head, N_l levels,
  *   N_p points per query, head and level, L = sum_l H_l * W_l.
- * Zero-sized dimensions are allowed (empty tensors).  Index limits:
- *   L * N_h * C_h, N_q * N_h * N_l * N_p * 2 and B * N_q * N_h must each be
- *   below 2^31. */
+ * Zero-sized dimensions are allowed (empty tensors).  Index limits (the
+ * kernels form element offsets in 32-bit arithmetic): (L + 2*max_l W_l + 4)
+ * * N_h * C_h, N_q * N_h * N_l * N_p * 2 and B * N_q * N_h must each be at
+ * most 2^31 - 1 (MSDA_ERR_TOO_LARGE otherwise; whole-quotient checks, so a
+ * size a few elements short of the bound may be refused too). */
 typedef struct msda_desc {
     int64_t B, N_q, N_h, C_h, N_l, N_p, L;
     const int64_t *spatial_shapes;    /* host, N_l pairs (H_l, W_l) */
