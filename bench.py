@@ -407,6 +407,30 @@ def run_ours(args, w: gen.Workload):
     staged_bwd_same = bool(torch.equal(gl_st, gl) and torch.equal(ga_st, ga))
     staged_bwd_first = msda.backward_staged_levels(desc)
 
+    # The backward for two output subsets (grad_value only: the tile-sorted
+    # path on dense problems; grad_sampling_locations + grad_attention_weights
+    # only), same protocol, outside the step.
+    def bwd_subset(flags):
+        msda.msda_backward(t["grad_output"], t["value"], data["spatial_shapes"], data["level_start_index"],
+                           t["sampling_locations"], t["attention_weights"], compute_grad_value=flags[0],
+                           compute_grad_sampling_locations=flags[1], compute_grad_attention_weights=flags[2],
+                           grad_value=gv_st if flags[0] else None, grad_sampling_locations=gl_st if flags[1] else None,
+                           grad_attention_weights=ga_st if flags[2] else None, workspace=ws, **kw)
+
+    subset_ms = {}
+    for name, flags in (("grad_value_only", (True, False, False)), ("loc_attn_only", (False, True, True))):
+        for _ in range(args.warmup):
+            flush.fill_(1.0)
+            bwd_subset(flags)
+        ev_s = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+        for i in range(K):
+            flush.fill_(float(i))
+            ev_s[i][0].record(stream)
+            bwd_subset(flags)
+            ev_s[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+        subset_ms[name] = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in ev_s), world, dev)
+
     # End to end: pinned host inputs -> device, forward, backward, results ->
     # pinned host, every step.  Two buffer sets and three streams pipeline the
     # steps the way a production loop would: the inputs of step i+1 are copied
@@ -528,6 +552,10 @@ def run_ours(args, w: gen.Workload):
             "speedup_vs_direct": round(fwd_mean / staged_ms, 4) if staged_ms > 0 else None,
             "staged_levels": list(range(staged_first, w.N_l)), "bit_identical_to_direct": staged_same,
             "timeouts": staged_timeouts},
+        "backward_subsets": {
+            "what": "msda_backward for two output subsets, same protocol, outside the step",
+            "grad_value_only_ms": round(subset_ms["grad_value_only"], 6),
+            "loc_attn_only_ms": round(subset_ms["loc_attn_only"], 6)},
         "backward_staged": {
             "what": "msda_backward_staged: grad_value of the coarse levels accumulated per block in shared memory",
             "bwd_ms": round(staged_bwd_ms, 6), "direct_bwd_ms": round(bwd_mean, 6),
