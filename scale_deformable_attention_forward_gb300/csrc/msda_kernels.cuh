@@ -397,6 +397,12 @@ __device__ __forceinline__ float2 row_softmax_stats(const float *attn, int64_t a
 #ifndef MSDA_BWD_MIN_BLOCKS
 #define MSDA_BWD_MIN_BLOCKS 3
 #endif
+#ifndef MSDA_FWD_LOOKAHEAD_BF16
+#define MSDA_FWD_LOOKAHEAD_BF16 1
+#endif
+#ifndef MSDA_FWD_LOOKAHEAD_F32
+#define MSDA_FWD_LOOKAHEAD_F32 0
+#endif
 #ifndef MSDA_FWD_MIN_BLOCKS_F32
 #define MSDA_FWD_MIN_BLOCKS_F32 3
 #endif
@@ -503,13 +509,34 @@ msda_forward_kernel(const __grid_constant__ Params p, const T *__restrict__ valu
 #pragma unroll
             for (int e = 0; e < VEC; ++e) acc[k][e] = 0.0f;
 
+        // LA: the next batch's location and weight are loaded before this batch is
+        // consumed (bfloat16 value: measured 4-9% faster; binary32: 2.6% slower)
+        constexpr bool LA = REC && (sizeof(T) == 2 ? MSDA_FWD_LOOKAHEAD_BF16 : MSDA_FWD_LOOKAHEAD_F32);
+        float nu = 0.0f, nv = 0.0f, nA = 0.0f;
+        if constexpr (LA) {
+            const int j = part * G + r;
+            if (j < NLP) {
+                nu = ldl(loc, lo + j * sJ, ldt);
+                nv = ldl(loc, lo + j * sJ + sXY, ldt);
+                nA = ldl(attn, ao + j, ldt);
+            }
+        }
         for (int j0 = part * G; j0 < NLP; j0 += jstep) {
             // owner phase: this lane's sample (past the last sample: weight 0 at offset 0)
             FwdCell mine = {0, 0, 0.0f, 0.0f, 0.0f, 0.0f};
             const int j = j0 + r;
+            float cu = nu, cv = nv, cA = nA;
+            if constexpr (LA) {
+                const int jn = j + jstep;
+                if (jn < NLP) {
+                    nu = ldl(loc, lo + jn * sJ, ldt);
+                    nv = ldl(loc, lo + jn * sJ + sXY, ldt);
+                    nA = ldl(attn, ao + jn, ldt);
+                }
+            }
             if (j < NLP) {
-                const float u = ldl(loc, lo + j * sJ, ldt), v = ldl(loc, lo + j * sJ + sXY, ldt);
-                float A = ldl(attn, ao + j, ldt);
+                const float u = LA ? cu : ldl(loc, lo + j * sJ, ldt), v = LA ? cv : ldl(loc, lo + j * sJ + sXY, ldt);
+                float A = LA ? cA : ldl(attn, ao + j, ldt);
                 if (logits) A = expf(A - sm.x) * sm.y;
                 const int l = (int)p.div_p.div((uint32_t)j);
                 const int W = lt.W[l], H = lt.H[l];
