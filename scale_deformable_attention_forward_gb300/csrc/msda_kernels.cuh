@@ -397,15 +397,6 @@ __device__ __forceinline__ float2 row_softmax_stats(const float *attn, int64_t a
 #ifndef MSDA_BWD_MIN_BLOCKS
 #define MSDA_BWD_MIN_BLOCKS 3
 #endif
-#ifndef MSDA_FWD_LOOKAHEAD_BF16
-#define MSDA_FWD_LOOKAHEAD_BF16 1
-#endif
-#ifndef MSDA_FWD_LOOKAHEAD_F32
-#define MSDA_FWD_LOOKAHEAD_F32 0
-#endif
-#ifndef MSDA_FWD_MIN_BLOCKS_F32
-#define MSDA_FWD_MIN_BLOCKS_F32 3
-#endif
 // Blocks per SM the row kernels are compiled for: for one 4-element chunk a
 // lane the forward 4 (64 registers a thread: more warps to hide the gather
 // latency) and the backward 3 (85 registers: its per-sample partials and
@@ -460,15 +451,14 @@ __device__ __forceinline__ FwdCell fwd_cell(const Cell &c, float A, int W, int H
 // reading each record (two 16-byte loads; rows of more than four chunks a
 // lane take the cell by shuffles instead), and loads every corner's channel
 // row with one instruction per channel chunk (lane r owns chunks r, r+G, ...),
-// two samples' corners in flight.  Binary32 rows of one chunk a lane run at
-// three blocks per SM (80 registers), bfloat16 at four: each measured best.
+// two samples' corners in flight; the next batch's location and weight are
+// loaded before the current batch is consumed.
 // PAD: 0 zeros, 1 border, -1 read p.padding at run time.  GEN: false for
 // binary32 weights (p.loc_dt == 0, p.logits == 0, the common case compiled
 // without the branches), true reads both at run time (with the backward's
 // register budget: the softmax statistics need registers).
 template <typename T, int VEC, int G, int NCH, int PAD, bool GEN, bool SPLIT>
-__global__ void __launch_bounds__(kThreads, (sizeof(T) == 4 && !GEN && NCH * VEC <= 4) ? MSDA_FWD_MIN_BLOCKS_F32
-                                                                                     : row_min_blocks(NCH *VEC, !GEN))
+__global__ void __launch_bounds__(kThreads, row_min_blocks(NCH *VEC, !GEN))
 msda_forward_kernel(const __grid_constant__ Params p, const T *__restrict__ value, const float *__restrict__ loc,
                     const float *__restrict__ attn, T *__restrict__ out) {
     __shared__ LevelTables lt;
@@ -510,8 +500,8 @@ msda_forward_kernel(const __grid_constant__ Params p, const T *__restrict__ valu
             for (int e = 0; e < VEC; ++e) acc[k][e] = 0.0f;
 
         // LA: the next batch's location and weight are loaded before this batch is
-        // consumed (bfloat16 value: measured 4-9% faster; binary32: 2.6% slower)
-        constexpr bool LA = REC && (sizeof(T) == 2 ? MSDA_FWD_LOOKAHEAD_BF16 : MSDA_FWD_LOOKAHEAD_F32);
+        // consumed (measured 1-9% faster)
+        constexpr bool LA = REC;
         float nu = 0.0f, nv = 0.0f, nA = 0.0f;
         if constexpr (LA) {
             const int j = part * G + r;
