@@ -73,7 +73,8 @@ __device__ __forceinline__ bool stage_wait(uint32_t bar, uint32_t phase) {
 }
 
 // One block: stage, then the forward of its queries (the direct kernel's
-// loop, binary32 weights, specialised padding).  A block whose copy has not
+// loop -- cell records in shared memory, the next batch's locations loaded
+// ahead -- binary32 weights, specialised padding).  A block whose copy has not
 // landed after kStageWaitLimit polls counts itself in *timeouts and gathers
 // every level from global memory (same results), then waits for the copy
 // again (bounded) before it exits.
@@ -88,6 +89,8 @@ msda_forward_staged_kernel(const __grid_constant__ Params p, const __grid_consta
     __shared__ __align__(8) uint64_t bar_mem;
     __shared__ LevelTables lt;
     __shared__ int sps[kMaxLevels];
+    __shared__ int4 rec_o[kThreads];
+    __shared__ float4 rec_w[kThreads];
     if (threadIdx.x < (unsigned)p.N_l) sps[threadIdx.x] = sp.sp[threadIdx.x];
     load_level_tables(p, lt);  // (ends with __syncthreads)
 
@@ -139,6 +142,9 @@ msda_forward_staged_kernel(const __grid_constant__ Params p, const __grid_consta
     for (int k = 0; k < NCH; ++k) nk += (k * G + r < p.chunks);
     const T *vbh = value + b * p.v_sB + (int64_t)h * p.v_sH + r * VEC;
     const uint32_t sbr = sbase + (uint32_t)(r * VEC * (int)sizeof(T));  // this lane's channels of shared pixel 0
+    int4 *wo = rec_o + (threadIdx.x & ~31);  // the warp's cell records, as in the direct kernel
+    float4 *ww = rec_w + (threadIdx.x & ~31);
+    const int mypos = rec_pos<G>(lane / G, r);
 
     // items as in the direct kernel: part `part` of query q takes its batches part, part + S, ...
     const int jstep = G << p.split_log2;
@@ -154,18 +160,42 @@ msda_forward_staged_kernel(const __grid_constant__ Params p, const __grid_consta
 #pragma unroll
             for (int e = 0; e < VEC; ++e) acc[k][e] = 0.0f;
 
+        // the next batch's location and weight are loaded before this batch is consumed
+        float nu = 0.0f, nv = 0.0f, nA = 0.0f;
+        {
+            const int jf = part * G + r;
+            if (jf < NLP) {
+                nu = ldl(loc, lo + jf * sJ, 0);
+                nv = ldl(loc, lo + jf * sJ + sXY, 0);
+                nA = ldl(attn, ao + jf, 0);
+            }
+        }
         for (int j0 = part * G; j0 < NLP; j0 += jstep) {
-            // owner phase: staged samples get offsets into shared memory (pixel stride C_h)
-            FwdCell mine = {0, 0, 0.0f, 0.0f, 0.0f, 0.0f};
+            // owner phase: the sample's record; staged samples get offsets into
+            // shared memory (pixel stride C_h), the others into value
             const int j = j0 + r;
+            const float u = nu, v = nv, A = nA;
+            {
+                const int jn = j + jstep;
+                if (jn < NLP) {
+                    nu = ldl(loc, lo + jn * sJ, 0);
+                    nv = ldl(loc, lo + jn * sJ + sXY, 0);
+                    nA = ldl(attn, ao + jn, 0);
+                }
+            }
             if (j < NLP) {
-                const float u = ldl(loc, lo + j * sJ, 0), v = ldl(loc, lo + j * sJ + sXY, 0);
-                const float A = ldl(attn, ao + j, 0);
                 const int l = (int)p.div_p.div((uint32_t)j);
                 const int W = lt.W[l], H = lt.H[l];
                 const Cell c = make_cell<PAD>(u, v, lt.sx[l], lt.sy[l], p.off, W, H, p.padding);
-                mine = j >= lsj ? fwd_cell(c, A, W, H, sps[l], C) : fwd_cell(c, A, W, H, lt.start[l], sP);
+                const Corners cr =
+                    j >= lsj ? corners_of(c, A, W, H, sps[l], C) : corners_of(c, A, W, H, lt.start[l], sP);
+                wo[mypos] = make_int4(cr.o[0], cr.o[1], cr.o[2], cr.o[3]);
+                ww[mypos] = make_float4(cr.w[0], cr.w[1], cr.w[2], cr.w[3]);
+            } else {  // past the row's last sample: weight 0 at value offset 0
+                wo[mypos] = make_int4(0, 0, 0, 0);
+                ww[mypos] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
             }
+            __syncwarp(gmask);
             const int ns = min(G, NLP - j0);
             constexpr int S2 = (G >= 2 && NCH * VEC <= 4) ? 2 : 1;  // two samples in flight for one chunk a lane
 #pragma unroll
@@ -176,21 +206,20 @@ msda_forward_staged_kernel(const __grid_constant__ Params p, const __grid_consta
                     float x[S2][4][NCH][VEC];
 #pragma unroll
                     for (int h2 = 0; h2 < S2; ++h2) {
-                        const int src = base + s + h2;
-                        const int o0 = __shfl_sync(gmask, mine.o0, src);
-                        const int o1 = __shfl_sync(gmask, mine.o1, src);
-                        w[h2][0] = __shfl_sync(gmask, mine.w00, src);
-                        w[h2][1] = __shfl_sync(gmask, mine.w01, src);
-                        w[h2][2] = __shfl_sync(gmask, mine.w10, src);
-                        w[h2][3] = __shfl_sync(gmask, mine.w11, src);
+                        const int qp = rec_pos<G>(lane / G, s + h2);
+                        const int4 o4 = wo[qp];
+                        const float4 w4 = ww[qp];
+                        o[h2][0] = o4.x;
+                        o[h2][1] = o4.y;
+                        o[h2][2] = o4.z;
+                        o[h2][3] = o4.w;
+                        w[h2][0] = w4.x;
+                        w[h2][1] = w4.y;
+                        w[h2][2] = w4.z;
+                        w[h2][3] = w4.w;
                         // the same for every lane of the warp; a sample past the row's last
                         // (weight 0, offset 0) reads global memory, as in the direct kernel
                         const bool st = j0 + s + h2 >= lsj && j0 + s + h2 < NLP;
-                        const int dx = (int)((unsigned)o0 >> 31) * (st ? C : sP);
-                        o[h2][0] = o0 & 0x7fffffff;
-                        o[h2][1] = (o0 & 0x7fffffff) + dx;
-                        o[h2][2] = o1;
-                        o[h2][3] = o1 + dx;
                         if (st) {
 #pragma unroll
                             for (int i = 0; i < 4; ++i)
@@ -219,6 +248,7 @@ msda_forward_staged_kernel(const __grid_constant__ Params p, const __grid_consta
                                         acc[k][e] = fmaf(w[h2][i], x[h2][i][k][e], acc[k][e]);
                 }
             }
+            __syncwarp(gmask);  // records are rewritten by the next batch
         }
         sum_parts<G, NCH, VEC>(acc, p.split_log2, lane);
         T *dst = out + (int64_t)bqh * C + r * VEC;
