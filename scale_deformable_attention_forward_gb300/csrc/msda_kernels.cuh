@@ -878,7 +878,7 @@ msda_backward_kernel(const __grid_constant__ Params p, const T *__restrict__ gra
 //   3. msda_tile_items_kernel   chunks[tile] = ceil(samples of tile / kChunk),
 //      scan                     then chunk offsets
 //   4. msda_tile_append_kernel  each partition block writes its samples'
-//                               entries (row | cell << 24, A, fx, fy) into its
+//                               entries (row | cell << 24, A - A fx, A fx, fy) into its
 //                               own slots of each tile (shared cursors)
 //   5. msda_tile_reduce_kernel  one block per chunk of a tile: counting sort of
 //                               the chunk's entries by cell in shared memory;
@@ -994,9 +994,11 @@ msda_tile_append_kernel(const __grid_constant__ Params p, const float *__restric
                 A = expf(A - m) * (1.0f / sum);
             }
             const uint32_t slot = (uint32_t)atomicAdd(cur + (int)(bh - bh0) * p.NB + tile, 1);
-            if (slot < p.capacity)
-                entries[slot] = make_uint4(bqh | ((uint32_t)cell << kEntryCellShift), __float_as_uint(A),
-                                           __float_as_uint(c.fx), __float_as_uint(c.fy));
+            if (slot < p.capacity) {
+                const float A1 = A * c.fx;  // the x factors of the corner weights, formed once per entry
+                entries[slot] = make_uint4(bqh | ((uint32_t)cell << kEntryCellShift), __float_as_uint(A - A1),
+                                           __float_as_uint(A1), __float_as_uint(c.fy));
+            }
         }
     }
 }
@@ -1141,9 +1143,8 @@ msda_tile_reduce_kernel(const __grid_constant__ Params p, const T *__restrict__ 
                     flush();
                     cur_cell = cell;
                 }
-                const float A = __uint_as_float(en.y), fx = __uint_as_float(en.z), fy = __uint_as_float(en.w);
-                const float A1 = A * fx;
-                const float ax0 = A - A1, ax1 = A1, ay0 = 1.0f - fy, ay1 = fy;
+                const float ax0 = __uint_as_float(en.y), ax1 = __uint_as_float(en.z), fy = __uint_as_float(en.w);
+                const float ay0 = 1.0f - fy, ay1 = fy;
                 const float w[4] = {ay0 * ax0, ay0 * ax1, ay1 * ax0, ay1 * ax1};
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
