@@ -13,7 +13,7 @@ dtypes.
 import numpy as np
 import pytest
 
-from parity_util import RTOL, assert_close, kw_of, np64, oracle_backward, to_device
+from parity_util import RTOL, assert_close, kw_of, np64, oracle_backward, tensor_groups, to_device
 from scale_deformable_attention_forward_gb300 import inputs as gen
 
 torch = pytest.importorskip("torch")
@@ -70,11 +70,14 @@ def test_two_calls_add_up(dtype, N_q):
             ref = oracle_backward(w, d, flags)
             total = total + ref[0]
             if flags[1]:
-                assert_close(np64(gl), ref[1], RTOL[(dtype, "bwd")], "grad_sampling_locations")
-                assert_close(np64(ga), ref[2], RTOL[(dtype, "bwd")], "grad_attention_weights")
+                assert_close(np64(gl), ref[1], RTOL[(dtype, "bwd")], "grad_sampling_locations",
+                             groups=tensor_groups(w, "grad_sampling_locations"))
+                assert_close(np64(ga), ref[2], RTOL[(dtype, "bwd")], "grad_attention_weights",
+                             groups=tensor_groups(w, "grad_attention_weights"))
             else:
                 assert gl is None and ga is None
-        assert_close(np64(acc), total, RTOL[("f32", "bwd")], f"accumulator {flags}")
+        assert_close(np64(acc), total, RTOL[("f32", "bwd")], f"accumulator {flags}",
+                     groups=tensor_groups(w, "grad_value"))
 
 
 @pytest.mark.parametrize("ll", ["BQHLP2", "B2QHLP"])
@@ -95,7 +98,7 @@ def test_query_chunks_sum_to_full_call(vl, ll):
         dc["grad_output"] = np.ascontiguousarray(d["grad_output"][:, q0:q1])
         _accumulate(wc, dc, to_device(dc, "f32"), acc, (True, False, False))
     torch.cuda.synchronize()
-    assert_close(np64(acc), full, RTOL[("f32", "bwd")], "chunked accumulator")
+    assert_close(np64(acc), full, RTOL[("f32", "bwd")], "chunked accumulator", groups=tensor_groups(w, "grad_value"))
 
 
 def test_rejects_misaligned_accumulator():

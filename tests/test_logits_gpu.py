@@ -7,7 +7,7 @@ Same tolerances as the weight-input entry points.
 """
 import pytest
 
-from parity_util import RTOL, assert_close, kw_of, np64, to_device
+from parity_util import RTOL, assert_close, kw_of, np64, tensor_groups, to_device
 from scale_deformable_attention_forward_gb300 import inputs as gen
 
 import oracle
@@ -38,7 +38,7 @@ def _check(w, flag_sets, check_forward=True):
         torch.cuda.synchronize()
         ref = oracle.forward_logits(d["value"], d["spatial_shapes"], d["level_start_index"], d["sampling_locations"],
                                     d["attention_logits"], coord_f32=True, **kw_of(w))
-        assert_close(np64(out), ref, RTOL[(w.dtype, "fwd")], f"{w.name} out")
+        assert_close(np64(out), ref, RTOL[(w.dtype, "fwd")], f"{w.name} out", groups=tensor_groups(w, "out"))
     for flags in flag_sets:
         got = msda.msda_backward_logits(t["grad_output"], t["value"], d["spatial_shapes"], d["level_start_index"],
                                         t["sampling_locations"], z, compute_grad_value=flags[0],
@@ -52,7 +52,8 @@ def _check(w, flag_sets, check_forward=True):
         for name, g, r, f in zip(("grad_value", "grad_sampling_locations", "grad_attention_logits"), got, ref,
                                  flags):
             if f:
-                assert_close(np64(g), r, RTOL[(w.dtype, "bwd")], f"{w.name} {name} flags={flags}")
+                grp = tensor_groups(w, "grad_attention_weights" if name == "grad_attention_logits" else name)
+                assert_close(np64(g), r, RTOL[(w.dtype, "bwd")], f"{w.name} {name} flags={flags}", groups=grp)
             else:
                 assert g is None
 

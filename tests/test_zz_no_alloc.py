@@ -1,4 +1,5 @@
-"""msda_backward_noalloc against msda_backward, through the C ABI (GPU).
+"""msda_backward_noalloc against the CPU oracle and against msda_backward,
+through the C ABI (GPU).
 
 msda_backward_noalloc serves callers that may not allocate device memory
 (for example a plug-in that must stay inside its host application's memory
@@ -12,7 +13,7 @@ import ctypes
 import numpy as np
 import pytest
 
-from parity_util import assert_close, np64, to_device
+from parity_util import assert_close, np64, oracle_backward, tensor_groups, to_device
 from scale_deformable_attention_forward_gb300 import inputs as gen
 
 torch = pytest.importorskip("torch")
@@ -79,14 +80,19 @@ def test_noalloc_matches_backward_twice(lib, name, dtype, flags):
     ref = _outs(t, flags)
     assert _call(lib, "backward", desc, t, ref, flags, ws, ws_bytes) == 0
     rtol = 2e-2 if dtype == "bf16" else 1e-4
+    oref = oracle_backward(w, d, tuple(bool(f) for f in flags))
+    names = ("grad_value", "grad_sampling_locations", "grad_attention_weights")
     for call in range(2):  # the second call starts from the first call's scratch contents
         got = _outs(t, flags)
         assert _call(lib, "noalloc", desc, t, got, flags) == 0
         torch.cuda.synchronize()
-        for g, r, n in zip(got, ref, ("grad_value", "grad_sampling_locations", "grad_attention_weights")):
+        for g, r, o, n in zip(got, ref, oref, names):
             if r is None:
+                assert o is None
                 continue
-            assert_close(np64(g), np64(r), rtol, f"call {call}: {n}")
+            grp = tensor_groups(w, n)
+            assert_close(np64(g), o, rtol, f"call {call}: {n} vs the oracle", groups=grp)
+            assert_close(np64(g), np64(r), rtol, f"call {call}: {n} vs msda_backward", groups=grp)
 
 
 def test_noalloc_refuses_oversized_accumulator(lib):
