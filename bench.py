@@ -15,9 +15,14 @@ interval of that step.  Under torchrun each rank runs an independent replica
 on its own GPU (the operator has no cross-GPU exchange); the value is the
 samples of all ranks divided by the slowest rank's time.
 
-``--impl reference`` times the CPU oracle (float64 C loops, one thread) on a
-bounded sample of the same workload: there is no GPU implementation to
-compare against.
+``--impl reference`` times the CPU oracle (float64 C loops, one process per
+host core) on a bounded sample of the same workload: there is no GPU
+implementation to compare against.  The default run also reports the
+oracle on one core (``cpu_baseline.single_thread``).
+
+Clocks: NVML is polled every millisecond on a host thread during the timed
+region (``clocks``; ``nvidia-smi`` at 100 ms is kept beside it), after a
+warm-up of at least W steps and at least ``--warmup-seconds`` of GPU work.
 """
 from __future__ import annotations
 
@@ -29,6 +34,7 @@ import platform
 import statistics
 import subprocess
 import sys
+import threading
 import time
 
 import numpy as np
@@ -42,7 +48,9 @@ from scale_deformable_attention_forward_gb300 import inputs as gen  # noqa: E402
 METRIC = "MSDA fwd+bwd Gsamples/s (q·h·l·p) and achieved HBM GB/s vs GB300 peak"
 UNIT = "Gsamples/s"
 FALLBACK_HBM_GBS = 6800.0
-REDUCTION_GBS = 6710.0  # measured binary32 red.global.add payload rate of a GB300
+# binary32 red.global.add payload rate of a GB300, measured with a reduction microbenchmark
+# (random 128-byte lines; the same for scalar, vector and TMA bulk reductions)
+REDUCTION_GBS = 6710.0
 CSRC = os.path.join(ROOT, "scale_deformable_attention_forward_gb300", "csrc")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")
 
@@ -147,6 +155,79 @@ class ClockSampler:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
                 "samples": len(sm)}
+
+
+class NvmlClockSampler:
+    """SM clock and clock-event reasons polled through NVML (ctypes on
+    libnvidia-ml) every `period` seconds on a host thread, so that even a
+    timed region of a few milliseconds gets samples.  Read-only queries."""
+
+    # nvmlClocksEventReason* bits (nvml.h); GPU idle and application-clock bits are not throttling
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, torch_device, period: float = 0.001):
+        self.period = period
+        self.samples = []
+        self.max_mhz = None
+        self.ok = False
+        self._stop = threading.Event()
+        self._thread = None
+        try:
+            import ctypes
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                return
+            h = ctypes.c_void_p()
+            found = False
+            try:  # the device whose UUID torch reports (NVML and CUDA may number devices differently)
+                import torch
+                uid = "GPU-" + str(torch.cuda.get_device_properties(torch_device).uuid)
+                found = nv.nvmlDeviceGetHandleByUUID(uid.encode(), ctypes.byref(h)) == 0
+            except Exception:
+                found = False
+            if not found and nv.nvmlDeviceGetHandleByIndex_v2(0, ctypes.byref(h)) != 0:
+                return
+            mx = ctypes.c_uint(0)
+            if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:  # 1 = NVML_CLOCK_SM
+                self.max_mhz = float(mx.value)
+            self._nv, self._h, self._ct = nv, h, ctypes
+            self.ok = True
+        except Exception:
+            self.ok = False
+
+    def _run(self):
+        nv, h, ct = self._nv, self._h, self._ct
+        clk, rs = ct.c_uint(0), ct.c_ulonglong(0)
+        while not self._stop.is_set():
+            if nv.nvmlDeviceGetClockInfo(h, 1, ct.byref(clk)) == 0 and \
+                    nv.nvmlDeviceGetCurrentClocksEventReasons(h, ct.byref(rs)) == 0:
+                self.samples.append((float(clk.value), int(rs.value)))
+            time.sleep(self.period)
+
+    def __enter__(self):
+        if self.ok:
+            self._thread = threading.Thread(target=self._run, daemon=True)
+            self._thread.start()
+        return self
+
+    def __exit__(self, *exc):
+        if self._thread is not None:
+            self._stop.set()
+            self._thread.join(timeout=5)
+        return False
+
+    def summary(self):
+        if not self.samples:
+            return None
+        reasons = set()
+        for _, bits in self.samples:
+            for b, n in self.REASONS.items():
+                if bits & b:
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(c for c, _ in self.samples), "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(reasons), "samples": len(self.samples),
+                "source": f"NVML every {self.period * 1e3:.0f} ms during the timed region"}
 
 
 # ----------------------------------------------------------------------------- distributed
@@ -330,15 +411,22 @@ def run_ours(args, w: gen.Workload):
                            t["sampling_locations"], t["attention_weights"], grad_value=gv,
                            grad_sampling_locations=gl, grad_attention_weights=ga, workspace=ws, **kw)
 
-    for _ in range(args.warmup):
-        flush.fill_(1.0)
-        fwd()
-        bwd()
-    torch.cuda.synchronize(dev)
+    # warm-up: W steps, and at least --warmup-seconds of GPU work so clocks settle
+    warm_done, t_warm = 0, time.perf_counter()
+    with ClockSampler(dev.index if dev.index is not None else 0) as clk_warm:
+        while warm_done < args.warmup or time.perf_counter() - t_warm < args.warmup_seconds:
+            flush.fill_(1.0)
+            fwd()
+            bwd()
+            warm_done += 1
+            if warm_done % 32 == 0:
+                torch.cuda.synchronize(dev)
+        torch.cuda.synchronize(dev)
 
     K = args.steps
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
-    with ClockSampler(dev.index if dev.index is not None else 0) as clk:
+    nvml = NvmlClockSampler(dev)
+    with ClockSampler(dev.index if dev.index is not None else 0) as clk, nvml:
         barrier(world)
         torch.cuda.synchronize(dev)
         wall0 = time.perf_counter()
@@ -355,6 +443,7 @@ def run_ours(args, w: gen.Workload):
     fwd_ms = [a.elapsed_time(b) for a, b, _ in ev]
     bwd_ms = [b.elapsed_time(c) for _, b, c in ev]
     step_ms_local = statistics.mean(f + b for f, b in zip(fwd_ms, bwd_ms))
+    step_med_local = statistics.median(f + b for f, b in zip(fwd_ms, bwd_ms))
     step_ms = max_over_ranks(step_ms_local, world, dev)
     value = w.samples * world / (step_ms * 1e-3) / 1e9
 
@@ -493,6 +582,10 @@ def run_ours(args, w: gen.Workload):
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / K_e2e, world, dev)
     barrier(world)
 
+    smi = clk.summary()
+    clocks = nvml.summary() or dict(smi, source="nvidia-smi every 100 ms during the timed region")
+    clocks["nvidia_smi"] = {"timed_region": smi, "warmup": clk_warm.summary()}
+
     fwd_b, bwd_b = compulsory_bytes(w)
     peak, peak_kind = measured_peaks()
     fwd_mean, bwd_mean = statistics.mean(fwd_ms), statistics.mean(bwd_ms)
@@ -521,8 +614,12 @@ def run_ours(args, w: gen.Workload):
                    "parallelism": f"replicas x{world} (no cross-GPU exchange)"},
         "fwd_ms": round(fwd_mean, 6),
         "bwd_ms": round(bwd_mean, 6),
+        "median": {"ms_per_step": round(max_over_ranks(step_med_local, world, dev), 6),
+                   "fwd_ms": round(statistics.median(fwd_ms), 6), "bwd_ms": round(statistics.median(bwd_ms), 6),
+                   "what": "medians over the K timed steps (value and ms_per_step use the mean)"},
         "wall_s_timed_region": round(wall, 3),
-        "clocks": clk.summary(),
+        "warmup_steps_run": warm_done,
+        "clocks": clocks,
         "e2e": {"value": round(w.samples * world / (e2e_ms * 1e-3) / 1e9, 4), "unit": UNIT,
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "path": "per step: pinned host -> device copies of the inputs, msda_forward, msda_backward, "
@@ -578,6 +675,11 @@ def run_ours(args, w: gen.Workload):
                       f"with all heads/levels/points, forward + backward x{reps} in float64; {samples} samples "
                       f"in {dt:.1f} s wall",
             "cpu": cpu_model()}
+        v1, samples1, n_q1, dt1, reps1 = time_oracle(w, args.workload, data, args.cpu_seconds / 3, 1)
+        result["cpu_baseline"]["single_thread"] = {
+            "value": round(v1, 6), "unit": UNIT, "cores": 1,
+            "sample": f"batch item 0: one process, queries [0, {n_q1}) of {w.n_queries} with all heads/levels/"
+                      f"points, forward + backward x{reps1} in float64; {samples1} samples in {dt1:.1f} s"}
     if rank == 0:
         print(json.dumps(result), flush=True)
     if world > 1:
@@ -639,6 +741,8 @@ def main(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--warmup-seconds", type=float, default=0.5,
+                    help="keep warming up (untimed) until this much wall time has passed")
     ap.add_argument("--workload", default="encoder32", choices=sorted(gen.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")

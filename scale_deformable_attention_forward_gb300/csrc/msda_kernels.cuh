@@ -161,18 +161,65 @@ __device__ __forceinline__ void red_add_v4(float *p, float a, float b, float c, 
 template <int VEC> struct RedIO;
 template <> struct RedIO<1> {
     static __device__ __forceinline__ void add(float *p, const float (&v)[1], float s) { red_add(p, s * v[0]); }
+    static __device__ __forceinline__ void add_sum(float *p, const float (&v)[1]) { red_add(p, v[0]); }
 };
+// s * v with packed binary32 products (rounded as the scalar products would be)
+__device__ __forceinline__ void red_add_scaled4(float *p, const float *v, float s) {
+    const float2 ss = make_float2(s, s);
+    const float2 lo = __fmul2_rn(ss, make_float2(v[0], v[1]));
+    const float2 hi = __fmul2_rn(ss, make_float2(v[2], v[3]));
+    red_add_v4(p, lo.x, lo.y, hi.x, hi.y);
+}
 template <> struct RedIO<4> {
-    static __device__ __forceinline__ void add(float *p, const float (&v)[4], float s) {
-        red_add_v4(p, s * v[0], s * v[1], s * v[2], s * v[3]);
+    static __device__ __forceinline__ void add(float *p, const float (&v)[4], float s) { red_add_scaled4(p, v, s); }
+    static __device__ __forceinline__ void add_sum(float *p, const float (&v)[4]) {
+        red_add_v4(p, v[0], v[1], v[2], v[3]);
     }
 };
 template <> struct RedIO<8> {
     static __device__ __forceinline__ void add(float *p, const float (&v)[8], float s) {
-        red_add_v4(p, s * v[0], s * v[1], s * v[2], s * v[3]);
-        red_add_v4(p + 4, s * v[4], s * v[5], s * v[6], s * v[7]);
+        red_add_scaled4(p, v, s);
+        red_add_scaled4(p + 4, v + 4, s);
+    }
+    static __device__ __forceinline__ void add_sum(float *p, const float (&v)[8]) {
+        red_add_v4(p, v[0], v[1], v[2], v[3]);
+        red_add_v4(p + 4, v[4], v[5], v[6], v[7]);
     }
 };
+
+// Packed binary32 arithmetic (sm_100 and later): one instruction applies an
+// FMA or a product to two lanes of data; each element is rounded exactly as
+// fmaf / a binary32 product would round it, so results are unchanged.
+// acc[e] += w * x[e] for the VEC elements of a chunk.
+template <int VEC>
+__device__ __forceinline__ void axpy(float (&acc)[VEC], float w, const float (&x)[VEC]) {
+    if constexpr (VEC % 2 == 0) {
+        const float2 ww = make_float2(w, w);
+#pragma unroll
+        for (int e = 0; e < VEC; e += 2) {
+            const float2 r = __ffma2_rn(ww, make_float2(x[e], x[e + 1]), make_float2(acc[e], acc[e + 1]));
+            acc[e] = r.x;
+            acc[e + 1] = r.y;
+        }
+    } else {
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) acc[e] = fmaf(w, x[e], acc[e]);
+    }
+}
+
+// dp += the products g[e] x[e] of one chunk, even channels into dp.x and odd
+// ones into dp.y (packed FMAs); <g, x> over a lane's chunks is dp.x + dp.y.
+template <int VEC>
+__device__ __forceinline__ void dot_acc(float2 &dp, const float (&g)[VEC], const float (&x)[VEC]) {
+    if constexpr (VEC % 2 == 0) {
+#pragma unroll
+        for (int e = 0; e < VEC; e += 2)
+            dp = __ffma2_rn(make_float2(g[e], g[e + 1]), make_float2(x[e], x[e + 1]), dp);
+    } else {
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) dp.x = fmaf(g[e], x[e], dp.x);
+    }
+}
 
 // Locations, attention weights and their gradients in their storage dtype
 // (dt: 0 binary32, 1 bfloat16, 2 binary16), addressed by element index from
@@ -569,10 +616,7 @@ msda_forward_kernel(const __grid_constant__ Params p, const T *__restrict__ valu
                             for (int i = 0; i < 4; ++i)
 #pragma unroll
                                 for (int kk = 0; kk < 2; ++kk)
-                                    if (k0 + kk < nk)
-#pragma unroll
-                                        for (int e = 0; e < VEC; ++e)
-                                            acc[k0 + kk][e] = fmaf(w[i], x[i][kk][e], acc[k0 + kk][e]);
+                                    if (k0 + kk < nk) axpy<VEC>(acc[k0 + kk], w[i], x[i][kk]);
                         }
                     }
                     continue;
@@ -607,10 +651,7 @@ msda_forward_kernel(const __grid_constant__ Params p, const T *__restrict__ valu
                         for (int i = 0; i < 4; ++i)
 #pragma unroll
                             for (int k = 0; k < NCH; ++k)
-                                if (k < nk)
-#pragma unroll
-                                    for (int e = 0; e < VEC; ++e)
-                                        acc[k][e] = fmaf(w[h2][i], x[h2][i][k][e], acc[k][e]);
+                                if (k < nk) axpy<VEC>(acc[k], w[h2][i], x[h2][i][k]);
                 }
             }
             if constexpr (REC) __syncwarp(gmask);  // records are rewritten by the next batch
@@ -662,6 +703,124 @@ __device__ __forceinline__ int bucket_of(const Cell &c, int bst, int BX, int *ce
     return bst + ty * BX + tx;
 }
 
+// ---------------------------------------------------------------- warp-aggregated grad_value
+// A warp serves four rows (neighbouring queries of one head) a batch of eight
+// samples each: 32 samples, up to 128 corner contributions A w_i g_row to
+// grad_value.  Neighbouring queries sample overlapping neighbourhoods, so many
+// of them land on the same pixel (encoder-ordered Deformable-DETR queries:
+// about half).  Instead of one 128-byte reduction line per contribution, the
+// warp first merges equal pixels in a table of its own in shared memory,
+// keyed by the pixel's element offset in the (b, h) slice and holding per
+// slot the summed corner weights of each of the four rows; a group then adds,
+// for every distinct pixel, the sum over the four rows of weight times that
+// row's grad_output with one red.global.add.v4.f32 per lane.  A contribution
+// that finds no slot within kAggProbes linear probes is added directly.  When
+// a batch has few repeated pixels (random locations), the warp scatters the
+// next kAggBackoff batches directly, as the plain kernel does, and then
+// measures again.
+constexpr int kAggSlots = 128;   // power of two
+constexpr int kAggProbes = 8;
+constexpr int kAggBackoff = 64;  // batches
+struct AggTable {
+    int key[kAggSlots];           // element offset of the pixel in the (b, h) slice; -1 empty
+    float4 w[kAggSlots];          // summed A w_i of rows 0..3 of the warp (x, y, z, w)
+    unsigned char list[128];      // slots filled in this batch, in fill order
+};
+__device__ __forceinline__ unsigned agg_hash(int key) {
+    return ((unsigned)key * 0x9E3779B1u) >> (32 - 7);  // 7 = log2(kAggSlots)
+}
+static_assert(kAggSlots == 128, "agg_hash takes the top 7 bits");
+
+// One batch of a warp's merged grad_value scatter (the AGG backward below);
+// every lane of the warp calls it.  (o4, w4): this lane's own sample record
+// (all weights 0 for no sample); g: chunk r of this lane's row of
+// grad_output; bqh / active: this lane's row and whether it has one.
+// Returns (contributions << 8) | distinct pixels of the batch.
+template <typename T>
+__device__ __forceinline__ int agg_scatter(AggTable &tab, int4 o4, float4 w4, int grp, int r, int nk, float *gbh,
+                                           const float (&g)[4], const T *grad_out, uint32_t bqh, bool active,
+                                           int C_h) {
+    const int lane = threadIdx.x & 31;
+    const int gbase = lane & ~7;
+    const unsigned below = (1u << lane) - 1u;
+    const unsigned gmask = 0xffu << gbase;
+    const int key4[4] = {o4.x, o4.y, o4.z, o4.w};
+    const float wt4[4] = {w4.x, w4.y, w4.z, w4.w};
+    // insert the four corners: the table sums each row's weights per pixel
+    int nrec = 0, ncon = 0;
+    unsigned ovf = 0;  // corners of this lane that found no slot
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const bool want = wt4[i] != 0.0f;
+        bool fresh = false;
+        unsigned s = 0;
+        if (want) {
+            bool placed = false;
+            s = agg_hash(key4[i]);
+            for (int t = 0; t < kAggProbes; ++t) {
+                const int old = atomicCAS(&tab.key[s], -1, key4[i]);
+                if (old == -1 || old == key4[i]) {
+                    placed = true;
+                    fresh = old == -1;
+                    break;
+                }
+                s = (s + 1) & (kAggSlots - 1);
+            }
+            if (placed) atomicAdd(reinterpret_cast<float *>(&tab.w[s]) + grp, wt4[i]);
+            else ovf |= 1u << i;
+        }
+        const unsigned nm = __ballot_sync(0xffffffffu, fresh);
+        if (fresh) tab.list[nrec + __popc(nm & below)] = (unsigned char)s;
+        nrec += __popc(nm);
+        ncon += __popc(__ballot_sync(0xffffffffu, want));
+    }
+    // contributions that found no slot: their row's group adds them directly
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        unsigned om = (__ballot_sync(0xffffffffu, (ovf >> i) & 1u) >> gbase) & 0xffu;
+        while (om) {  // uniform over the group
+            const int src = gbase + __ffs(om) - 1;
+            om &= om - 1;
+            const int key = __shfl_sync(gmask, key4[i], src);
+            const float wt = __shfl_sync(gmask, wt4[i], src);
+            if (nk) RedIO<4>::add(gbh + key, g, wt);
+        }
+    }
+    // chunk r of the four rows' grad_output (zero for a group without a row)
+    float G4[4][4];
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+        const uint32_t rb = __shfl_sync(0xffffffffu, bqh, b * 8);
+        const bool ab = __shfl_sync(0xffffffffu, (int)active, b * 8) != 0;
+        if (ab && nk) {
+            VecIO<T, 4>::load(grad_out + (int64_t)rb * C_h + r * 4, G4[b]);
+        } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) G4[b][e] = 0.0f;
+        }
+    }
+    __syncwarp();
+    // one reduction line per distinct pixel; group grp takes every fourth
+    for (int t = grp; t < nrec; t += 4) {
+        const int s = tab.list[t];
+        const int key = tab.key[s];
+        const float4 ws = tab.w[s];
+        float a[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        axpy<4>(a, ws.x, G4[0]);
+        axpy<4>(a, ws.y, G4[1]);
+        axpy<4>(a, ws.z, G4[2]);
+        axpy<4>(a, ws.w, G4[3]);
+        if (nk) red_add_v4(gbh + key, a[0], a[1], a[2], a[3]);
+    }
+    __syncwarp();
+    for (int t = lane; t < nrec; t += 32) {  // empty the slots for the next batch
+        const int s = tab.list[t];
+        tab.key[s] = -1;
+        tab.w[s] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    }
+    return (ncon << 8) | nrec;
+}
+
 // The backward reuses the forward's work split: a group of G lanes per row,
 // samples taken G at a time, lane r computing sample j0 + r's cell once and
 // publishing its record (corner offsets, weights A w_i).  With grad_output's
@@ -673,20 +832,23 @@ __device__ __forceinline__ int bucket_of(const Cell &c, int bst, int BX, int *ce
 //   <g, dS/dx> = sum_i dw_i/dx d_i     -> grad_sampling_locations.x = A sx <g, dS/dx>
 //   <g, dS/dy> = sum_i dw_i/dy d_i     -> grad_sampling_locations.y = A sy <g, dS/dy>
 // (corners outside the map read 0: their d_i count as 0).  grad_value, when
-// requested here, receives A w_i g at corner i straight into the binary32
-// accumulator, one red.global.add.v4.f32 per lane and corner (the
-// tile-sorted grad_value runs this kernel without kGradValue).
+// requested here, receives A w_i g at corner i in the binary32 accumulator:
+// AGG = false, one red.global.add.v4.f32 per lane and corner; AGG = true
+// (four rows a warp, one chunk a lane), merged per warp and batch as above.
+// (The tile-sorted grad_value runs this kernel without kGradValue.)
 // FL: kGradValue|kGradLoc|kGradAttn or kGradValue (exactly these outputs),
 // kGradLoc|kGradAttn (no grad_value; the two others as p.flags says), or -1
 // (everything from p.flags at run time).  PAD as in the forward.
-template <typename T, int VEC, int G, int NCH, int PAD, int FL, bool SPLIT>
+template <typename T, int VEC, int G, int NCH, int PAD, int FL, bool SPLIT, bool AGG>
 __global__ void __launch_bounds__(kThreads, row_min_blocks(NCH *VEC, false))
 msda_backward_kernel(const __grid_constant__ Params p, const T *__restrict__ grad_out, const T *__restrict__ value,
                      const float *__restrict__ loc, const float *__restrict__ attn, float *__restrict__ gv_acc,
                      float *__restrict__ grad_loc, float *__restrict__ grad_attn) {
+    static_assert(!AGG || (G == 8 && NCH == 1 && VEC == 4 && !SPLIT), "aggregation: four rows a warp, one chunk a lane");
     __shared__ LevelTables lt;
     __shared__ int4 rec_o[kThreads];
     __shared__ float4 rec_w[kThreads];
+    __shared__ AggTable agg_tables[AGG ? kThreads / 32 : 1];
     load_level_tables(p, lt);
     constexpr int GPB = kThreads / G;
     const int flags = FL < 0 ? p.flags : (FL == (kGradLoc | kGradAttn) ? (p.flags & FL) : FL);
@@ -710,9 +872,23 @@ msda_backward_kernel(const __grid_constant__ Params p, const T *__restrict__ gra
     const int slog = SPLIT ? p.split_log2 : 0;
     const RowRange rr = block_rows<GPB>(p, slog);
     const int jstep = G << slog;
+    AggTable &tab = agg_tables[AGG ? (threadIdx.x >> 5) : 0];
+    if constexpr (AGG) {
+        for (int i = lane; i < kAggSlots; i += 32) {
+            tab.key[i] = -1;
+            tab.w[i] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        }
+        __syncwarp();
+    }
+    int direct_left = 0;  // (AGG) batches the warp still scatters directly
 
-    for (uint32_t item = rr.beg + threadIdx.x / G; item < rr.end; item += rr.step) {
-        const uint32_t row = item >> slog;
+    // AGG: the four groups of a warp run the same iterations (warp-wide
+    // exchanges); a group past the last row runs along without samples.
+    for (uint32_t lead = rr.beg + (AGG ? (threadIdx.x >> 5) * (32 / G) : threadIdx.x / G); lead < rr.end;
+         lead += rr.step) {
+        const uint32_t item = AGG ? lead + grp : lead;
+        const bool active = !AGG || item < rr.end;
+        const uint32_t row = (active ? item : lead) >> slog;
         const int part = (int)(item & ((1u << slog) - 1u));
         const Row rw = decode_row(p, row);
         const int64_t bhoff = rw.b * p.v_sB + (int64_t)rw.h * p.v_sH;
@@ -737,11 +913,20 @@ msda_backward_kernel(const __grid_constant__ Params p, const T *__restrict__ gra
                 }
             }
         }
+        // (AGG) the warp's rows share one (b, h) slice, so pixel offsets are
+        // comparable keys; a warp straddling two heads scatters directly
+        bool merge = false;
+        if constexpr (AGG) {
+            const uint32_t bh = rw.b * (uint32_t)p.N_h + rw.h;
+            const uint32_t bh0 = __shfl_sync(0xffffffffu, bh, 0);  // every lane takes part in the shuffle
+            merge = __all_sync(0xffffffffu, !active || bh == bh0) && scatter;
+        }
 
         for (int j0 = part * G; j0 < NLP; j0 += jstep) {
+            const bool agg_now = AGG && merge && direct_left == 0;  // uniform over the warp
             // owner phase: this lane's sample
             const int j = j0 + r;
-            const bool live = j < NLP;
+            const bool live = active && j < NLP;
             int l = 0;
             float A = 0.0f;
             Cell c;
@@ -761,9 +946,10 @@ msda_backward_kernel(const __grid_constant__ Params p, const T *__restrict__ gra
                 wo[mypos] = make_int4(cr.o[0], cr.o[1], cr.o[2], cr.o[3]);
                 ww[mypos] = make_float4(cr.w[0], cr.w[1], cr.w[2], cr.w[3]);
             }
-            __syncwarp(gmask);
+            if constexpr (AGG) __syncwarp();
+            else __syncwarp(gmask);
             // consume phase: the group's samples in order
-            const int ns = min(G, NLP - j0);
+            const int ns = active ? min(G, NLP - j0) : 0;
             float pd[4][G <= 8 ? G : 1];  // this lane's part of d_i, per sample of the batch
             float dt[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // (G > 8) totals of this lane's own sample
 #pragma unroll
@@ -776,6 +962,8 @@ msda_backward_kernel(const __grid_constant__ Params p, const T *__restrict__ gra
                     if (need_v) {
                         // (wide rows: two chunks' corners at a time; each d_i still sums chunk by chunk)
                         constexpr int KB = NCH > 2 ? 2 : NCH;
+                        // d_i in two interleaved partial sums (even and odd channels) by packed FMAs
+                        float2 dp[4] = {{0.0f, 0.0f}, {0.0f, 0.0f}, {0.0f, 0.0f}, {0.0f, 0.0f}};
 #pragma unroll
                         for (int k0 = 0; k0 < NCH; k0 += KB) {
                             float x[4][KB][VEC];
@@ -788,12 +976,12 @@ msda_backward_kernel(const __grid_constant__ Params p, const T *__restrict__ gra
                             for (int i = 0; i < 4; ++i)
 #pragma unroll
                                 for (int kk = 0; kk < KB; ++kk)
-                                    if (k0 + kk < nk)
-#pragma unroll
-                                        for (int e = 0; e < VEC; ++e) d[i] = fmaf(g[k0 + kk][e], x[i][kk][e], d[i]);
+                                    if (k0 + kk < nk) dot_acc<VEC>(dp[i], g[k0 + kk], x[i][kk]);
                         }
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) d[i] = dp[i].x + dp[i].y;
                     }
-                    if (scatter) {
+                    if (scatter && !agg_now) {
                         const float4 w4 = ww[q];
                         const float wv[4] = {w4.x, w4.y, w4.z, w4.w};
 #pragma unroll
@@ -818,7 +1006,6 @@ msda_backward_kernel(const __grid_constant__ Params p, const T *__restrict__ gra
                     }
                 }
             }
-            __syncwarp(gmask);  // records are rewritten by the next batch
             if (need_v) {
                 if constexpr (G <= 8) {
 #pragma unroll
@@ -846,8 +1033,21 @@ msda_backward_kernel(const __grid_constant__ Params p, const T *__restrict__ gra
                     }
                 }
             }
+            if constexpr (AGG) {
+                if (agg_now) {
+                    const int nc = agg_scatter<T>(tab, wo[mypos], ww[mypos], grp, r, nk, gbh, g[0], grad_out, rw.bqh,
+                                                  active, p.C_h);
+                    // nc: (contributions << 8) | distinct pixels of this batch
+                    if ((nc & 0xff) * 5 > (nc >> 8) * 4) direct_left = kAggBackoff;  // under 1.25 per pixel
+                } else if (direct_left > 0) {
+                    --direct_left;
+                }
+                __syncwarp();  // records are rewritten by the next batch
+            } else {
+                __syncwarp(gmask);
+            }
         }
-        if (soft && want_ga) {
+        if (soft && want_ga && active) {
             // d/dlogit_j = A_j (<g, S_j> - sum_k A_k <g, S_k>); lane r rewrites the
             // samples it stored above
 #pragma unroll
@@ -1113,7 +1313,7 @@ msda_tile_reduce_kernel(const __grid_constant__ Params p, const T *__restrict__ 
                 float *dst = gb + (int64_t)(p.start[l] + y * W + x) * p.v_sP;
 #pragma unroll
                 for (int k = 0; k < NCH; ++k)
-                    if (k < nk) RedIO<VEC>::add(dst + k * G * VEC, acc[i][k], 1.0f);
+                    if (k < nk) RedIO<VEC>::add_sum(dst + k * G * VEC, acc[i][k]);
             }
 #pragma unroll
             for (int k = 0; k < NCH; ++k)

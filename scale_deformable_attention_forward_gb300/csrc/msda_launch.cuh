@@ -46,11 +46,14 @@ cudaError_t fwd_launch(const Params &p, const T *value, const float *loc, const 
     return cudaGetLastError();
 }
 
+// The forward always runs the instantiation with the row split compiled in:
+// with split_log2 = 0 it takes whole rows, and unlike the split-free
+// instantiation (its batch loop with a constant step) it compiles without
+// spills for one and two chunks a lane (binary32 and bfloat16).
 template <typename T, int V, int GG, int NN, int PAD, bool GEN>
 cudaError_t fwd_split(const Params &p, const T *value, const float *loc, const float *attn, T *out,
                       cudaStream_t stream) {
-    return p.split_log2 > 0 ? fwd_launch<T, V, GG, NN, PAD, GEN, true>(p, value, loc, attn, out, stream)
-                            : fwd_launch<T, V, GG, NN, PAD, GEN, false>(p, value, loc, attn, out, stream);
+    return fwd_launch<T, V, GG, NN, PAD, GEN, true>(p, value, loc, attn, out, stream);
 }
 
 template <typename T, int V, int GG, int NN>
@@ -83,12 +86,21 @@ cudaError_t launch_forward_path(const Params &p, int G, int NCH, const T *value,
     return cudaErrorInvalidConfiguration;
 }
 
+// The warp-aggregated grad_value scatter (msda_backward_kernel, AGG) serves
+// the 32-channel-row shape (8 lanes, one 4-element chunk a lane) whenever the
+// kernel adds grad_value; MSDA_BWD_AGGREGATE=0 builds the plain scatter only.
+#ifndef MSDA_BWD_AGGREGATE
+#define MSDA_BWD_AGGREGATE 1
+#endif
+
 template <typename T, int V, int GG, int NN, int PAD, int FL, bool SPLIT>
 cudaError_t bwd_launch(const Params &p, const T *grad_out, const T *value, const float *loc, const float *attn,
                        const BwdBuffers &bb, cudaStream_t stream) {
     Params q = p;
     if (!SPLIT) q.split_log2 = 0;
-    auto kernel = msda_backward_kernel<T, V, GG, NN, PAD, FL, SPLIT>;
+    constexpr bool AGG = MSDA_BWD_AGGREGATE && GG == 8 && NN == 1 && V == 4 && PAD >= 0 && !SPLIT &&
+                         FL != (kGradLoc | kGradAttn);
+    auto kernel = msda_backward_kernel<T, V, GG, NN, PAD, FL, SPLIT, AGG>;
     const unsigned blocks = row_grid(kernel, GG, q);
     kernel<<<blocks, kThreads, 0, stream>>>(q, grad_out, value, loc, attn, bb.gv_acc, bb.grad_loc, bb.grad_attn);
     return cudaGetLastError();

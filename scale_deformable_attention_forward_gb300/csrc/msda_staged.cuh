@@ -242,10 +242,7 @@ msda_forward_staged_kernel(const __grid_constant__ Params p, const __grid_consta
                         for (int i = 0; i < 4; ++i)
 #pragma unroll
                             for (int k = 0; k < NCH; ++k)
-                                if (k < nk)
-#pragma unroll
-                                    for (int e = 0; e < VEC; ++e)
-                                        acc[k][e] = fmaf(w[h2][i], x[h2][i][k][e], acc[k][e]);
+                                if (k < nk) axpy<VEC>(acc[k], w[h2][i], x[h2][i][k]);
                 }
             }
             __syncwarp(gmask);  // records are rewritten by the next batch
@@ -387,13 +384,15 @@ msda_backward_staged_kernel(const __grid_constant__ Params p, const __grid_const
 #pragma unroll
                             for (int k = 0; k < NCH; ++k)
                                 if (k < nk) VecIO<T, VEC>::load(vbh + oo[i] + k * G * VEC, x[i][k]);
+                        // the direct kernel's summation: even / odd channel partial sums, chunk by chunk
 #pragma unroll
-                        for (int i = 0; i < 4; ++i)
+                        for (int i = 0; i < 4; ++i) {
+                            float2 dp = make_float2(0.0f, 0.0f);
 #pragma unroll
                             for (int k = 0; k < NCH; ++k)
-                                if (k < nk)
-#pragma unroll
-                                    for (int e = 0; e < VEC; ++e) d[i] = fmaf(g[k][e], x[i][k][e], d[i]);
+                                if (k < nk) dot_acc<VEC>(dp, g[k], x[i][k]);
+                            d[i] = dp.x + dp.y;
+                        }
                     }
                     const float4 w4 = ww[qp];
                     const float wv[4] = {w4.x, w4.y, w4.z, w4.w};
@@ -481,7 +480,7 @@ msda_backward_staged_kernel(const __grid_constant__ Params p, const __grid_const
                         v[e] = acc_s[px * C + cc * VEC + e];
                         any |= v[e] != 0.0f;
                     }
-                    if (any) RedIO<VEC>::add(gbh + (lt.start[l] + pl) * sP + k * G * VEC, v, 1.0f);
+                    if (any) RedIO<VEC>::add_sum(gbh + (lt.start[l] + pl) * sP + k * G * VEC, v);
                 }
         }
     }
