@@ -94,7 +94,9 @@ enum msda_status {
     MSDA_ERR_UNSUPPORTED = -8,  /* a valid but unimplemented combination (value_dtype F16,
                                    C_h > 256 with unaligned pointers) */
     MSDA_ERR_MISALIGNED = -9,   /* a pointer not aligned to its element size */
-    MSDA_ERR_CUDA = -10         /* the CUDA runtime reported an error (msda_last_cuda_error) */
+    MSDA_ERR_CUDA = -10,        /* the CUDA runtime reported an error (msda_last_cuda_error) */
+    MSDA_ERR_STAGE_COPY = -11   /* msda_staged_timeouts: a staged-forward block exited while its
+                                   shared-memory copy was still in flight (see there) */
 };
 
 /* Levels the descriptor may describe. */
@@ -155,9 +157,14 @@ int msda_forward_staged(const msda_desc *desc, const void *value, const void *sa
                         const void *attention_weights, void *out, cudaStream_t stream);
 
 /* The number of staged-forward blocks, since the library was loaded, that
- * gave up waiting for their shared-memory copy (expected 0), in *count.
- * Synchronises with the device.  Returns MSDA_OK, MSDA_ERR_NULL_POINTER or
- * MSDA_ERR_CUDA. */
+ * gave up waiting for their shared-memory copy (expected 0), in *count.  Such
+ * a block gathers from global memory instead (same results) and waits for the
+ * copy once more, bounded, before it exits; if that wait runs out too, the
+ * copy may still write into shared memory that a later block on the same
+ * multiprocessor owns, and this call returns MSDA_ERR_STAGE_COPY (the staged
+ * outputs produced since are suspect; *count is still written).  Synchronises
+ * with the device.  Returns MSDA_OK, MSDA_ERR_STAGE_COPY,
+ * MSDA_ERR_NULL_POINTER or MSDA_ERR_CUDA. */
 int msda_staged_timeouts(unsigned int *count);
 
 /* The first level msda_forward_staged stages for this descriptor (levels

@@ -53,6 +53,9 @@ class msda_desc(ctypes.Structure):
                 ("loc_dtype", ctypes.c_int32)]
 
 
+STATUS_STAGE_COPY = -11  # msda_staged_timeouts: a staged block exited with its copy in flight
+
+
 class MSDAError(RuntimeError):
     """A non-zero status returned by libmsda."""
 
@@ -297,7 +300,9 @@ def staged_levels(desc) -> int:
 
 def staged_timeouts() -> int:
     """Staged-forward blocks (since the library was loaded) that gave up
-    waiting for their shared-memory copy; synchronises with the device."""
+    waiting for their shared-memory copy; synchronises with the device.
+    Raises MSDAError (status STATUS_STAGE_COPY) if such a block exited while
+    its copy was still in flight."""
     lib = load_library()
     n = ctypes.c_uint(0)
     rc = lib.msda_staged_timeouts(ctypes.byref(n))

@@ -678,8 +678,9 @@ int backward_entry(const msda_desc *desc, const void *grad_output, const void *v
     return record_cuda(e);
 }
 
-// Blocks of the staged forward that gave up waiting for their copy.
-__device__ unsigned int g_stage_timeouts = 0;
+// Blocks of the staged forward that gave up waiting for their copy [0], and
+// of those, blocks that exited while the copy was still unfinished [1].
+__device__ unsigned int g_stage_timeouts[2] = {0u, 0u};
 
 // The counter's device address on the current device, looked up once per
 // device (null when the lookup fails).
@@ -700,7 +701,11 @@ unsigned int *stage_timeout_counter() {
 
 int staged_timeouts(unsigned int *count) {
     if (!count) return MSDA_ERR_NULL_POINTER;
-    return record_cuda(cudaMemcpyFromSymbol(count, g_stage_timeouts, sizeof(unsigned int)));
+    unsigned int c[2] = {0u, 0u};
+    const int rc = record_cuda(cudaMemcpyFromSymbol(c, g_stage_timeouts, sizeof(c)));
+    if (rc != MSDA_OK) return rc;
+    *count = c[0];
+    return c[1] ? MSDA_ERR_STAGE_COPY : MSDA_OK;
 }
 
 int forward_entry(const msda_desc *desc, const void *value, const void *sampling_locations,
@@ -873,6 +878,9 @@ const char *msda_status_string(int status) {
     case MSDA_ERR_UNSUPPORTED: return "valid but unsupported combination (binary16 value, or C_h > 256 unaligned)";
     case MSDA_ERR_MISALIGNED: return "a pointer is not aligned to its element size";
     case MSDA_ERR_CUDA: return "the CUDA runtime reported an error (see msda_last_cuda_error)";
+    case MSDA_ERR_STAGE_COPY:
+        return "a staged-forward block exited before its shared-memory copy landed; staged results since "
+               "then are suspect";
     default: return "unknown status";
     }
 }

@@ -75,9 +75,10 @@ __device__ __forceinline__ bool stage_wait(uint32_t bar, uint32_t phase) {
 // One block: stage, then the forward of its queries (the direct kernel's
 // loop -- cell records in shared memory, the next batch's locations loaded
 // ahead -- binary32 weights, specialised padding).  A block whose copy has not
-// landed after kStageWaitLimit polls counts itself in *timeouts and gathers
+// landed after kStageWaitLimit polls counts itself in timeouts[0] and gathers
 // every level from global memory (same results), then waits for the copy
-// again (bounded) before it exits.
+// again (bounded) before it exits, counting itself in timeouts[1] if that
+// wait runs out too.
 template <typename T, int VEC, int G, int NCH, int PAD>
 __global__ void __launch_bounds__(kThreads, MSDA_STAGED_MIN_BLOCKS)
 msda_forward_staged_kernel(const __grid_constant__ Params p, const __grid_constant__ StagePlan sp,
@@ -255,8 +256,14 @@ msda_forward_staged_kernel(const __grid_constant__ Params p, const __grid_consta
                 if (k < nk) VecIO<T, VEC>::store(dst + k * G * VEC, acc[k]);
         }
     }
-    // a copy that had not landed must not write into shared memory the next block owns
-    if (staging && !ok) stage_wait(bar, 0);
+    // a copy that had not landed must not write into shared memory the next
+    // block owns: wait for it again (bounded); if it still has not landed, the
+    // block exits with the copy in flight and counts itself in timeouts[1]
+    // (msda_staged_timeouts then reports MSDA_ERR_STAGE_COPY)
+    if (staging && !ok) {
+        const bool landed_late = __syncthreads_and(stage_wait(bar, 0));
+        if (!landed_late && threadIdx.x == 0) atomicAdd(timeouts + 1, 1u);
+    }
 }
 
 // ---------------------------------------------------------------- staged backward

@@ -39,11 +39,21 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_status_strings(lib):
-    for code in range(-10, 1):
+    for code in range(-11, 1):
         s = msda.msda_status_string(code)
         assert s and s != "unknown status"
     assert msda.msda_status_string(-99) == "unknown status"
     assert lib.msda_last_cuda_error() == 0
+
+
+def test_staged_copy_status_reaches_the_caller(lib):
+    """MSDA_ERR_STAGE_COPY (a staged-forward block exited with its copy in
+    flight, reported by msda_staged_timeouts) has its own code and message,
+    and the binding turns it into an exception naming it.  (The condition
+    itself needs a copy that never lands, which no test provokes on a GPU.)"""
+    assert msda.STATUS_STAGE_COPY == -11
+    err = msda.MSDAError(msda.STATUS_STAGE_COPY, "msda_staged_timeouts")
+    assert "shared-memory copy" in str(err) and "-11" in str(err)
 
 
 LEVELS = ((4, 6), (2, 3))
