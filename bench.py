@@ -447,6 +447,19 @@ def run_ours(args, w: gen.Workload):
     step_ms = max_over_ranks(step_ms_local, world, dev)
     value = w.samples * world / (step_ms * 1e-3) / 1e9
 
+    if args.only_step:  # (profiling runs: the step alone, no other legs)
+        smi = clk.summary()
+        if rank == 0:
+            print(json.dumps({"metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world,
+                              "steps": K, "warmup": args.warmup, "ms_per_step": round(step_ms, 6),
+                              "fwd_ms": round(statistics.mean(fwd_ms), 6), "bwd_ms": round(statistics.mean(bwd_ms), 6),
+                              "config": {"name": args.workload}, "only_step": True,
+                              "clocks": nvml.summary() or smi}), flush=True)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+
     # The staged-level forward (msda_forward_staged) under the same protocol,
     # outside the step: the same output as msda_forward, a different gather.
     out_st = torch.empty_like(out)
@@ -495,6 +508,34 @@ def run_ours(args, w: gen.Workload):
     staged_bwd_ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in ev_sb), world, dev)
     staged_bwd_same = bool(torch.equal(gl_st, gl) and torch.equal(ga_st, ga))
     staged_bwd_first = msda.backward_staged_levels(desc)
+
+    # The backward with plain per-corner atomics (the warp-aggregated scatter
+    # switched off through MSDA_BWD_AGGREGATE=0), same protocol, outside the step.
+    prev = os.environ.get("MSDA_BWD_AGGREGATE")
+    os.environ["MSDA_BWD_AGGREGATE"] = "0"
+    try:
+        for _ in range(args.warmup):
+            flush.fill_(1.0)
+            bwd_plain_out = msda.msda_backward(t["grad_output"], t["value"], data["spatial_shapes"],
+                                               data["level_start_index"], t["sampling_locations"],
+                                               t["attention_weights"], grad_value=gv_st, grad_sampling_locations=gl_st,
+                                               grad_attention_weights=ga_st, workspace=ws, **kw)
+        ev_pl = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+        for i in range(K):
+            flush.fill_(float(i))
+            ev_pl[i][0].record(stream)
+            msda.msda_backward(t["grad_output"], t["value"], data["spatial_shapes"], data["level_start_index"],
+                               t["sampling_locations"], t["attention_weights"], grad_value=gv_st,
+                               grad_sampling_locations=gl_st, grad_attention_weights=ga_st, workspace=ws, **kw)
+            ev_pl[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+    finally:
+        if prev is None:
+            del os.environ["MSDA_BWD_AGGREGATE"]
+        else:
+            os.environ["MSDA_BWD_AGGREGATE"] = prev
+    plain_bwd_ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in ev_pl), world, dev)
+    plain_same = bool(torch.equal(gl_st, gl) and torch.equal(ga_st, ga))
 
     # The backward for two output subsets (grad_value only: the tile-sorted
     # path on dense problems; grad_sampling_locations + grad_attention_weights
@@ -638,10 +679,11 @@ def run_ours(args, w: gen.Workload):
         # C_h values per sample), against the reduction rate a microbenchmark of red.global.add
         # measured on this GPU (6.7 TB/s of payload, whatever the request shape).
         "roofline_reduction": {
-            "what": "grad_value reduction payload (samples x 4 corners x C_h x 4 B) / backward time",
-            "achieved": round(w.samples * 4 * w.C_h * 4 / (bwd_mean * 1e-3) / 1e9, 1),
+            "what": "grad_value reduction payload (samples x 4 corners x C_h x 4 B) / backward time of the "
+                    "plain-atomics leg (one reduction line per corner and sample)",
+            "achieved": round(w.samples * 4 * w.C_h * 4 / (plain_bwd_ms * 1e-3) / 1e9, 1),
             "peak": REDUCTION_GBS, "unit": "GB/s",
-            "frac": round(w.samples * 4 * w.C_h * 4 / (bwd_mean * 1e-3) / 1e9 / REDUCTION_GBS, 4),
+            "frac": round(w.samples * 4 * w.C_h * 4 / (plain_bwd_ms * 1e-3) / 1e9 / REDUCTION_GBS, 4),
             "peak_source": "red.global.add.v4.f32 microbenchmark on GB300 (random 128-byte lines)"},
         "forward_staged": {
             "what": "msda_forward_staged: coarse levels copied to shared memory by TMA, gathered from there",
@@ -659,6 +701,12 @@ def run_ours(args, w: gen.Workload):
             "speedup_vs_direct": round(bwd_mean / staged_bwd_ms, 4) if staged_bwd_ms > 0 else None,
             "staged_levels": list(range(staged_bwd_first, w.N_l)),
             "loc_attn_grads_bit_identical_to_direct": staged_bwd_same},
+        "backward_plain_atomics": {
+            "what": "msda_backward with the warp-aggregated grad_value scatter off (MSDA_BWD_AGGREGATE=0): one "
+                    "red.global.add.v4.f32 line per corner and sample",
+            "bwd_ms": round(plain_bwd_ms, 6), "aggregated_bwd_ms": round(bwd_mean, 6),
+            "aggregated_speedup": round(plain_bwd_ms / bwd_mean, 4) if bwd_mean > 0 else None,
+            "loc_attn_grads_bit_identical": plain_same},
         "roofline_step": {
             "what": "forward + backward compulsory bytes / step time",
             "achieved": round((fwd_b + bwd_b) / (step_ms * 1e-3) / 1e9, 1), "peak": peak, "unit": "GB/s",
@@ -746,6 +794,9 @@ def main(argv=None):
     ap.add_argument("--workload", default="encoder32", choices=sorted(gen.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only-step", action="store_true",
+                    help="time the step and print a short line; skip the staged, subset, end-to-end and CPU legs "
+                         "(for profiler runs)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="CPU work for the cpu_baseline leg (a slice of the workload)")
     ap.add_argument("--reference-seconds", type=float, default=90.0,

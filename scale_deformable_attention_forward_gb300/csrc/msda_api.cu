@@ -9,6 +9,7 @@
 
 #include <cudaTypedefs.h>
 #include <limits.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include <atomic>
@@ -262,6 +263,13 @@ BwdPlan plan_backward(const msda_desc *d, int compute_grad_value, bool allow_sor
 // only while rows x lanes fill at most half of the GPU's resident threads
 // (2048 a multiprocessor), every part keeps at least one batch of G samples
 // and a row's parts stay within one warp.
+// The warp-aggregated grad_value scatter is on unless the environment
+// variable MSDA_BWD_AGGREGATE is "0" (read at every backward call).
+int aggregate_enabled() {
+    const char *v = getenv("MSDA_BWD_AGGREGATE");
+    return (v && v[0] == '0' && v[1] == '\0') ? 0 : 1;
+}
+
 int choose_split(const Params &p, int G, bool allowed) {
     if (!allowed || p.rows == 0) return 0;
     const uint64_t capacity = (uint64_t)(p.n_sm > 0 ? p.n_sm : 1) * 2048;
@@ -624,6 +632,7 @@ int backward_entry(const msda_desc *desc, const void *grad_output, const void *v
     p.logits = mode.logits ? 1 : 0;
     p.n_sm = samples > 0 ? sm_count() : 0;
     p.split_log2 = choose_split(p, cfg.G, !mode.logits);  // the logits' gradient needs whole rows
+    p.aggregate = aggregate_enabled();
 
     cudaError_t e = cudaSuccess;
     if (fv && !accumulate) e = launch_zero_f32(bb.gv_acc, value_elems, stream);

@@ -60,6 +60,7 @@ struct Params {
     int logits;     // 1: `attention_weights` holds logits; A = softmax over the row's N_l*N_p of them
     int loc_dt;     // dtype of locations, weights and their gradients: 0 binary32, 1 bfloat16, 2 binary16
     int split_log2; // row kernels: each row's samples split over 2^split_log2 groups (see block_rows)
+    int aggregate;  // backward: warp-aggregated grad_value scatter where the kernel shape has one
     // value (and grad_value / accumulator) element strides
     int64_t v_sB;
     int v_sH, v_sP;

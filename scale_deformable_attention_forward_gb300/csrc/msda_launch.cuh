@@ -88,22 +88,27 @@ cudaError_t launch_forward_path(const Params &p, int G, int NCH, const T *value,
 
 // The warp-aggregated grad_value scatter (msda_backward_kernel, AGG) serves
 // the 32-channel-row shape (8 lanes, one 4-element chunk a lane) whenever the
-// kernel adds grad_value; MSDA_BWD_AGGREGATE=0 builds the plain scatter only.
-#ifndef MSDA_BWD_AGGREGATE
-#define MSDA_BWD_AGGREGATE 1
-#endif
+// kernel adds grad_value and p.aggregate is set (the default; the environment
+// variable MSDA_BWD_AGGREGATE=0 selects the plain per-corner atomics).
+template <typename T, int V, int GG, int NN, int PAD, int FL, bool SPLIT, bool AGG>
+cudaError_t bwd_launch_agg(const Params &q, const T *grad_out, const T *value, const float *loc, const float *attn,
+                           const BwdBuffers &bb, cudaStream_t stream) {
+    auto kernel = msda_backward_kernel<T, V, GG, NN, PAD, FL, SPLIT, AGG>;
+    const unsigned blocks = row_grid(kernel, GG, q);
+    kernel<<<blocks, kThreads, 0, stream>>>(q, grad_out, value, loc, attn, bb.gv_acc, bb.grad_loc, bb.grad_attn);
+    return cudaGetLastError();
+}
 
 template <typename T, int V, int GG, int NN, int PAD, int FL, bool SPLIT>
 cudaError_t bwd_launch(const Params &p, const T *grad_out, const T *value, const float *loc, const float *attn,
                        const BwdBuffers &bb, cudaStream_t stream) {
     Params q = p;
     if (!SPLIT) q.split_log2 = 0;
-    constexpr bool AGG = MSDA_BWD_AGGREGATE && GG == 8 && NN == 1 && V == 4 && PAD >= 0 && !SPLIT &&
-                         FL != (kGradLoc | kGradAttn);
-    auto kernel = msda_backward_kernel<T, V, GG, NN, PAD, FL, SPLIT, AGG>;
-    const unsigned blocks = row_grid(kernel, GG, q);
-    kernel<<<blocks, kThreads, 0, stream>>>(q, grad_out, value, loc, attn, bb.gv_acc, bb.grad_loc, bb.grad_attn);
-    return cudaGetLastError();
+    constexpr bool CAN_AGG = GG == 8 && NN == 1 && V == 4 && PAD >= 0 && !SPLIT && FL != (kGradLoc | kGradAttn);
+    if constexpr (CAN_AGG) {
+        if (q.aggregate) return bwd_launch_agg<T, V, GG, NN, PAD, FL, SPLIT, true>(q, grad_out, value, loc, attn, bb, stream);
+    }
+    return bwd_launch_agg<T, V, GG, NN, PAD, FL, SPLIT, false>(q, grad_out, value, loc, attn, bb, stream);
 }
 
 // p.flags: the outputs this launch produces (without kGradValue when the

@@ -368,3 +368,30 @@ def test_cuda_graph_capture(dtype):
         assert torch.equal(cap[k], eager[k]), k
     for k in ("gv", "gv1", "gv_st"):
         assert_close(np64(cap[k]), np64(eager[k]), RTOL[(dtype, "bwd")], f"{k} replay")
+
+
+# ------------------------------------------------------------------ plain atomics
+@pytest.mark.parametrize("name", ["encoder32", "hires16"])
+def test_plain_atomics_full_size(name, monkeypatch):
+    """The backward with the warp-aggregated grad_value scatter switched off
+    (MSDA_BWD_AGGREGATE=0: one reduction per corner and sample), against the
+    oracle at full size."""
+    monkeypatch.setenv("MSDA_BWD_AGGREGATE", "0")
+    check_workload(gen.WORKLOADS[name], flag_sets=[(True, True, True)], check_forward=False)
+
+
+# Enough rows (B * N_h * N_q > 9.7 K on 152 multiprocessors) that the
+# whole-row kernels run, not the row split of small problems: the
+# aggregated scatter and, switched off, the plain atomics of the same shape.
+def _whole_rows(dtype, vl, ll, align, pad, seed):
+    return _small(dtype, vl, ll, align, pad, N_q=701, N_h=8, B=2, seed=seed)
+
+
+@pytest.mark.parametrize("aggregate", ["1", "0"])
+@pytest.mark.parametrize("vl,ll", [("BLNC", "BQHLP2"), ("BNLC", "B2QHLP")])
+@pytest.mark.parametrize("pad,align", [("zeros", False), ("border", True)])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_whole_row_scatter_matrix(dtype, pad, align, vl, ll, aggregate, monkeypatch):
+    monkeypatch.setenv("MSDA_BWD_AGGREGATE", aggregate)
+    check_workload(_whole_rows(dtype, vl, ll, align, pad, seed=17),
+                   flag_sets=[(True, True, True), (True, True, False), (True, False, True)], check_forward=False)
