@@ -20,7 +20,7 @@ host core) on a bounded sample of the same workload: there is no GPU
 implementation to compare against.  The default run also reports the
 oracle on one core (``cpu_baseline.single_thread``).
 
-Clocks: NVML is polled every millisecond on a host thread during the timed
+Clocks: NVML is polled every millisecond by a child process during the timed
 region (``clocks``; ``nvidia-smi`` at 100 ms is kept beside it), after a
 warm-up of at least W steps and at least ``--warmup-seconds`` of GPU work.
 """
@@ -34,7 +34,6 @@ import platform
 import statistics
 import subprocess
 import sys
-import threading
 import time
 
 import numpy as np
@@ -157,10 +156,39 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+_NVML_CHILD = r"""
+import ctypes, sys, time
+uuid, period = sys.argv[1], float(sys.argv[2])
+nv = ctypes.CDLL("libnvidia-ml.so.1")
+if nv.nvmlInit_v2() != 0:
+    print("fail", flush=True); sys.exit(0)
+h = ctypes.c_void_p()
+if not uuid or nv.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(h)) != 0:
+    if nv.nvmlDeviceGetHandleByIndex_v2(0, ctypes.byref(h)) != 0:
+        print("fail", flush=True); sys.exit(0)
+mx = ctypes.c_uint(0)
+nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx))  # 1 = NVML_CLOCK_SM
+print("ready", mx.value, flush=True)
+clk, rs = ctypes.c_uint(0), ctypes.c_ulonglong(0)
+out = []
+import select
+while True:
+    if select.select([sys.stdin], [], [], 0)[0]:
+        break
+    if nv.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0 and \
+            nv.nvmlDeviceGetCurrentClocksEventReasons(h, ctypes.byref(rs)) == 0:
+        out.append("%.6f %d %d" % (time.time(), clk.value, rs.value))
+    time.sleep(period)
+print("\n".join(out), flush=True)
+"""
+
+
 class NvmlClockSampler:
     """SM clock and clock-event reasons polled through NVML (ctypes on
-    libnvidia-ml) every `period` seconds on a host thread, so that even a
-    timed region of a few milliseconds gets samples.  Read-only queries."""
+    libnvidia-ml, read-only queries) every `period` seconds by a child
+    process, so that even a timed region of a few milliseconds gets samples
+    and the timed process's host thread is not slowed by the polling.
+    Samples are kept when their timestamps fall inside the `with` block."""
 
     # nvmlClocksEventReason* bits (nvml.h); GPU idle and application-clock bits are not throttling
     REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
@@ -170,51 +198,42 @@ class NvmlClockSampler:
         self.period = period
         self.samples = []
         self.max_mhz = None
-        self.ok = False
-        self._stop = threading.Event()
-        self._thread = None
+        self.proc = None
         try:
-            import ctypes
-            nv = ctypes.CDLL("libnvidia-ml.so.1")
-            if nv.nvmlInit_v2() != 0:
-                return
-            h = ctypes.c_void_p()
-            found = False
-            try:  # the device whose UUID torch reports (NVML and CUDA may number devices differently)
-                import torch
-                uid = "GPU-" + str(torch.cuda.get_device_properties(torch_device).uuid)
-                found = nv.nvmlDeviceGetHandleByUUID(uid.encode(), ctypes.byref(h)) == 0
-            except Exception:
-                found = False
-            if not found and nv.nvmlDeviceGetHandleByIndex_v2(0, ctypes.byref(h)) != 0:
-                return
-            mx = ctypes.c_uint(0)
-            if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:  # 1 = NVML_CLOCK_SM
-                self.max_mhz = float(mx.value)
-            self._nv, self._h, self._ct = nv, h, ctypes
-            self.ok = True
+            import torch
+            uid = "GPU-" + str(torch.cuda.get_device_properties(torch_device).uuid)
         except Exception:
-            self.ok = False
-
-    def _run(self):
-        nv, h, ct = self._nv, self._h, self._ct
-        clk, rs = ct.c_uint(0), ct.c_ulonglong(0)
-        while not self._stop.is_set():
-            if nv.nvmlDeviceGetClockInfo(h, 1, ct.byref(clk)) == 0 and \
-                    nv.nvmlDeviceGetCurrentClocksEventReasons(h, ct.byref(rs)) == 0:
-                self.samples.append((float(clk.value), int(rs.value)))
-            time.sleep(self.period)
+            uid = ""
+        try:
+            self.proc = subprocess.Popen([sys.executable, "-c", _NVML_CHILD, uid, str(period)], stdin=subprocess.PIPE,
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            first = self.proc.stdout.readline().split()
+            if not first or first[0] != "ready":
+                self.proc.kill()
+                self.proc = None
+            else:
+                self.max_mhz = float(first[1]) if len(first) > 1 and float(first[1]) > 0 else None
+        except Exception:
+            self.proc = None
 
     def __enter__(self):
-        if self.ok:
-            self._thread = threading.Thread(target=self._run, daemon=True)
-            self._thread.start()
+        self.t0 = time.time()
         return self
 
     def __exit__(self, *exc):
-        if self._thread is not None:
-            self._stop.set()
-            self._thread.join(timeout=5)
+        t1 = time.time()
+        if self.proc is not None:
+            try:
+                out, _ = self.proc.communicate(input="stop\n", timeout=30)
+            except Exception:
+                self.proc.kill()
+                out = ""
+            for line in out.splitlines():
+                parts = line.split()
+                if len(parts) == 3:
+                    t, c, r = float(parts[0]), float(parts[1]), int(parts[2])
+                    if self.t0 <= t <= t1:
+                        self.samples.append((c, r))
         return False
 
     def summary(self):
@@ -227,7 +246,7 @@ class NvmlClockSampler:
                     reasons.add(n)
         return {"sm_mhz": statistics.median(c for c, _ in self.samples), "sm_max_mhz": self.max_mhz,
                 "reasons": sorted(reasons), "samples": len(self.samples),
-                "source": f"NVML every {self.period * 1e3:.0f} ms during the timed region"}
+                "source": f"NVML every {self.period * 1e3:.0f} ms during the timed region (a child process)"}
 
 
 # ----------------------------------------------------------------------------- distributed
