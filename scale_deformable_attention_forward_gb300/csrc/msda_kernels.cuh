@@ -504,8 +504,11 @@ __device__ __forceinline__ FwdCell fwd_cell(const Cell &c, float A, int W, int H
 // PAD: 0 zeros, 1 border, -1 read p.padding at run time.  GEN: false for
 // binary32 weights (p.loc_dt == 0, p.logits == 0, the common case compiled
 // without the branches), true reads both at run time (with the backward's
-// register budget: the softmax statistics need registers).
-template <typename T, int VEC, int G, int NCH, int PAD, bool GEN, bool SPLIT>
+// register budget: the softmax statistics need registers).  FULL: every
+// batch holds G samples (N_l*N_p a multiple of G) and every lane owns all NCH
+// chunks (C_h = G*NCH*VEC), so the partial-batch and masked-lane guards
+// compile away.
+template <typename T, int VEC, int G, int NCH, int PAD, bool GEN, bool SPLIT, bool FULL>
 __global__ void __launch_bounds__(kThreads, row_min_blocks(NCH *VEC, !GEN))
 msda_forward_kernel(const __grid_constant__ Params p, const T *__restrict__ value, const float *__restrict__ loc,
                     const float *__restrict__ attn, T *__restrict__ out) {
@@ -523,9 +526,9 @@ msda_forward_kernel(const __grid_constant__ Params p, const T *__restrict__ valu
     float4 *ww = rec_w + (REC ? (threadIdx.x & ~31) : 0);
     const int mypos = rec_pos<G>(lane / G, r);
     const int sP = p.v_sP, sJ = p.l_sJ, sXY = p.l_sXY, NLP = p.NLP;
-    int nk = 0;  // chunks this lane owns: k*G + r < chunks
+    int nk = 0;  // chunks this lane owns: k*G + r < chunks (FULL: all NCH)
 #pragma unroll
-    for (int k = 0; k < NCH; ++k) nk += (k * G + r < p.chunks);
+    for (int k = 0; k < NCH; ++k) nk += (FULL || k * G + r < p.chunks);
     const int slog = SPLIT ? p.split_log2 : 0;  // (SPLIT = false: the whole-row kernel, no split code)
     const RowRange rr = block_rows<GPB>(p, slog);
     const int jstep = G << slog;
@@ -592,7 +595,7 @@ msda_forward_kernel(const __grid_constant__ Params p, const T *__restrict__ valu
             }
             if constexpr (REC) __syncwarp(gmask);
             // consume phase: the group's samples in order, corners of two in flight
-            const int ns = min(G, NLP - j0);
+            const int ns = FULL ? G : min(G, NLP - j0);  // (FULL: every batch has G samples)
             constexpr int S2 = (G >= 2 && NCH * VEC <= 4) ? 2 : 1;  // two samples in flight for one chunk a lane
 #pragma unroll
             for (int s = 0; s < G; s += S2) {
@@ -839,8 +842,8 @@ __device__ __forceinline__ int agg_scatter(AggTable &tab, int4 o4, float4 w4, in
 // (The tile-sorted grad_value runs this kernel without kGradValue.)
 // FL: kGradValue|kGradLoc|kGradAttn or kGradValue (exactly these outputs),
 // kGradLoc|kGradAttn (no grad_value; the two others as p.flags says), or -1
-// (everything from p.flags at run time).  PAD as in the forward.
-template <typename T, int VEC, int G, int NCH, int PAD, int FL, bool SPLIT, bool AGG>
+// (everything from p.flags at run time).  PAD and FULL as in the forward.
+template <typename T, int VEC, int G, int NCH, int PAD, int FL, bool SPLIT, bool AGG, bool FULL>
 __global__ void __launch_bounds__(kThreads, row_min_blocks(NCH *VEC, false))
 msda_backward_kernel(const __grid_constant__ Params p, const T *__restrict__ grad_out, const T *__restrict__ value,
                      const float *__restrict__ loc, const float *__restrict__ attn, float *__restrict__ gv_acc,
@@ -866,9 +869,9 @@ msda_backward_kernel(const __grid_constant__ Params p, const T *__restrict__ gra
     float4 *ww = rec_w + (threadIdx.x & ~31);
     const int mypos = rec_pos<G>(grp, r);
     const int sP = p.v_sP, sJ = p.l_sJ, sXY = p.l_sXY, NLP = p.NLP;
-    int nk = 0;  // chunks this lane owns: k*G + r < chunks
+    int nk = 0;  // chunks this lane owns: k*G + r < chunks (FULL: all NCH)
 #pragma unroll
-    for (int k = 0; k < NCH; ++k) nk += (k * G + r < p.chunks);
+    for (int k = 0; k < NCH; ++k) nk += (FULL || k * G + r < p.chunks);
     // split only without logits (the rewrite below needs whole rows); SPLIT = false: no split code
     const int slog = SPLIT ? p.split_log2 : 0;
     const RowRange rr = block_rows<GPB>(p, slog);
@@ -927,7 +930,7 @@ msda_backward_kernel(const __grid_constant__ Params p, const T *__restrict__ gra
             const bool agg_now = AGG && merge && direct_left == 0;  // uniform over the warp
             // owner phase: this lane's sample
             const int j = j0 + r;
-            const bool live = active && j < NLP;
+            const bool live = active && (FULL || j < NLP);
             int l = 0;
             float A = 0.0f;
             Cell c;
@@ -950,7 +953,7 @@ msda_backward_kernel(const __grid_constant__ Params p, const T *__restrict__ gra
             if constexpr (AGG) __syncwarp();
             else __syncwarp(gmask);
             // consume phase: the group's samples in order
-            const int ns = active ? min(G, NLP - j0) : 0;
+            const int ns = active ? (FULL ? G : min(G, NLP - j0)) : 0;
             float pd[4][G <= 8 ? G : 1];  // this lane's part of d_i, per sample of the batch
             float dt[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // (G > 8) totals of this lane's own sample
 #pragma unroll
