@@ -843,8 +843,11 @@ __device__ __forceinline__ int agg_scatter(AggTable &tab, int4 o4, float4 w4, in
 // FL: kGradValue|kGradLoc|kGradAttn or kGradValue (exactly these outputs),
 // kGradLoc|kGradAttn (no grad_value; the two others as p.flags says), or -1
 // (everything from p.flags at run time).  PAD and FULL as in the forward.
+#ifndef MSDA_AGG_MIN_BLOCKS
+#define MSDA_AGG_MIN_BLOCKS MSDA_BWD_MIN_BLOCKS
+#endif
 template <typename T, int VEC, int G, int NCH, int PAD, int FL, bool SPLIT, bool AGG, bool FULL>
-__global__ void __launch_bounds__(kThreads, row_min_blocks(NCH *VEC, false))
+__global__ void __launch_bounds__(kThreads, AGG ? MSDA_AGG_MIN_BLOCKS : row_min_blocks(NCH *VEC, false))
 msda_backward_kernel(const __grid_constant__ Params p, const T *__restrict__ grad_out, const T *__restrict__ value,
                      const float *__restrict__ loc, const float *__restrict__ attn, float *__restrict__ gv_acc,
                      float *__restrict__ grad_loc, float *__restrict__ grad_attn) {

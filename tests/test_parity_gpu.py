@@ -383,15 +383,19 @@ def test_plain_atomics_full_size(name, monkeypatch):
 # Enough rows (B * N_h * N_q > 9.7 K on 152 multiprocessors) that the
 # whole-row kernels run, not the row split of small problems: the
 # aggregated scatter and, switched off, the plain atomics of the same shape.
-def _whole_rows(dtype, vl, ll, align, pad, seed):
-    return _small(dtype, vl, ll, align, pad, N_q=701, N_h=8, B=2, seed=seed)
+# N_p = 4 (16 samples a row, C_h = 32): full rows, the guard-free kernels;
+# N_p = 3: a partial last batch, the guarded ones.
+def _whole_rows(dtype, vl, ll, align, pad, seed, N_p=3):
+    return _small(dtype, vl, ll, align, pad, N_q=701, N_h=8, B=2, N_p=N_p, seed=seed)
 
 
+@pytest.mark.parametrize("N_p", [3, 4])
 @pytest.mark.parametrize("aggregate", ["1", "0"])
 @pytest.mark.parametrize("vl,ll", [("BLNC", "BQHLP2"), ("BNLC", "B2QHLP")])
 @pytest.mark.parametrize("pad,align", [("zeros", False), ("border", True)])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-def test_whole_row_scatter_matrix(dtype, pad, align, vl, ll, aggregate, monkeypatch):
+def test_whole_row_scatter_matrix(dtype, pad, align, vl, ll, aggregate, N_p, monkeypatch):
     monkeypatch.setenv("MSDA_BWD_AGGREGATE", aggregate)
-    check_workload(_whole_rows(dtype, vl, ll, align, pad, seed=17),
-                   flag_sets=[(True, True, True), (True, True, False), (True, False, True)], check_forward=False)
+    check_workload(_whole_rows(dtype, vl, ll, align, pad, seed=17 + N_p, N_p=N_p),
+                   flag_sets=[(True, True, True), (True, True, False), (True, False, True), (False, True, True)],
+                   check_forward=N_p == 4)
