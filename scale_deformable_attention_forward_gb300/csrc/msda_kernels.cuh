@@ -21,9 +21,11 @@
 // the group through swizzled shared-memory records (wide forward rows: by
 // shuffles).  The backward sums its per-sample dot products over
 // the G lanes with a transposed butterfly and scatters grad_value with vector
-// atomics (red.global.add.v4.f32), or, for grad_value-only calls on dense
-// problems, through the tile-sorted path further down.  The staged variants
-// (coarse levels in shared memory) are in msda_staged.cuh.
+// atomics (red.global.add.v4.f32) -- for 32-channel rows after merging the
+// contributions of a warp's four rows that land on one pixel -- or, for
+// grad_value-only calls on dense problems, through the tile-sorted path
+// further down.  The staged variants (coarse levels in shared memory) are in
+// msda_staged.cuh.
 #pragma once
 
 #include <cuda_runtime.h>
