@@ -692,6 +692,24 @@ __device__ __forceinline__ float reduce_scatter(float (&v)[G], int r, unsigned g
     return v[0];
 }
 
+// The steps o = N/2, ..., 1 of reduce_scatter on the N = G/2 values left
+// after its first step (o = G/2), which the backward takes as soon as each
+// pair of samples t, t + G/2 is done (fewer partials live at once).
+template <int N>
+__device__ __forceinline__ float reduce_scatter_tail(float (&v)[N], int r, unsigned gmask) {
+#pragma unroll
+    for (int o = N / 2; o >= 1; o >>= 1) {
+        const bool up = (r & o) != 0;
+#pragma unroll
+        for (int t = 0; t < o; ++t) {
+            const float send = up ? v[t] : v[t + o];
+            const float keep = up ? v[t + o] : v[t];
+            v[t] = keep + __shfl_xor_sync(gmask, send, o);
+        }
+    }
+    return v[0];
+}
+
 // Tiles of the tile-sorted grad_value.  A sample's cell (top-left corner
 // (y0, x0), y0 in [-1, H-1], x0 in [-1, W-1]) has extended coordinates
 // (ey, ex) = (y0 + 1, x0 + 1) on an (H+1) x (W+1) grid, cut into tiles of
@@ -957,12 +975,18 @@ msda_backward_kernel(const __grid_constant__ Params p, const T *__restrict__ gra
             }
             if constexpr (AGG) __syncwarp();
             else __syncwarp(gmask);
-            // consume phase: the group's samples in order
+            // consume phase: the group's samples, in order or (PAIRED) in pairs
+            // t, t + G/2, whose first butterfly exchange is taken at once
             const int ns = active ? (FULL ? G : min(G, NLP - j0)) : 0;
-            float pd[4][G <= 8 ? G : 1];  // this lane's part of d_i, per sample of the batch
-            float dt[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // (G > 8) totals of this lane's own sample
+            // (measured: the full backward 6-8% faster; without grad_value, 2-3% slower)
+            constexpr bool PAIRED = G == 8 && FL != (kGradLoc | kGradAttn);
+            float pd[4][(G <= 8 && !PAIRED) ? G : 1];  // this lane's part of d_i, per sample of the batch
+            float ph[4][PAIRED ? G / 2 : 1];           // (PAIRED) the same after the first exchange
+            float dprev[4] = {0.0f, 0.0f, 0.0f, 0.0f}; // (PAIRED) sample t of the pair being formed
+            float dt[4] = {0.0f, 0.0f, 0.0f, 0.0f};    // (G > 8) totals of this lane's own sample
 #pragma unroll
-            for (int s = 0; s < G; ++s) {
+            for (int u = 0; u < G; ++u) {
+                const int s = PAIRED ? ((u >> 1) + (u & 1) * (G / 2)) : u;
                 float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
                 if (s < ns) {
                     const int q = rec_pos<G>(grp, s);
@@ -1001,7 +1025,21 @@ msda_backward_kernel(const __grid_constant__ Params p, const T *__restrict__ gra
                                     if (k < nk) RedIO<VEC>::add(gbh + oo[i] + k * G * VEC, g[k], wv[i]);
                     }
                 }
-                if constexpr (G <= 8) {
+                if constexpr (PAIRED) {
+                    if (!(u & 1)) {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) dprev[i] = d[i];
+                    } else if (need_v) {  // reduce_scatter's first step for samples t and t + G/2
+                        const int t = u >> 1;
+                        const bool up = (r & (G / 2)) != 0;
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const float send = up ? dprev[i] : d[i];
+                            const float keep = up ? d[i] : dprev[i];
+                            ph[i][t] = keep + __shfl_xor_sync(gmask, send, G / 2);
+                        }
+                    }
+                } else if constexpr (G <= 8) {
 #pragma unroll
                     for (int i = 0; i < 4; ++i) pd[i][s] = d[i];
                 } else if (need_v) {  // wide groups: sum per sample, the owner keeps it
@@ -1016,7 +1054,10 @@ msda_backward_kernel(const __grid_constant__ Params p, const T *__restrict__ gra
                 }
             }
             if (need_v) {
-                if constexpr (G <= 8) {
+                if constexpr (PAIRED) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) dt[i] = reduce_scatter_tail<G / 2>(ph[i], r, gmask);
+                } else if constexpr (G <= 8) {
 #pragma unroll
                     for (int i = 0; i < 4; ++i) dt[i] = reduce_scatter<G>(pd[i], r, gmask);
                 }

@@ -110,8 +110,8 @@ cudaError_t bwd_launch_full(const Params &q, const T *grad_out, const T *value, 
 // Full rows (every batch G samples, every lane all NCH chunks): the
 // guard-free instantiation, for the padding-specialised whole-row kernels with
 // the aggregated scatter or without grad_value (measured faster: encoder32 1-2%,
-// hires16 6%, encoder16 1.5%; the plain-scatter and row-split instantiations
-// spill 70-100 bytes without the guards and keep them).
+// hires16 6%, encoder16 1.5%); the plain-scatter and row-split kernels keep the
+// guards (measured no faster without them).
 #ifndef MSDA_BWD_FULL
 #define MSDA_BWD_FULL 1
 #endif
