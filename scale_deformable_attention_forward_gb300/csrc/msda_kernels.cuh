@@ -1143,6 +1143,9 @@ msda_backward_kernel(const __grid_constant__ Params p, const T *__restrict__ gra
 // gather and is faster.
 // Within a (tile, part) segment entries are in shared-atomic order, so
 // grad_value's summation order (not its value) varies from call to call.
+#ifndef MSDA_REDUCE_ROWS
+#define MSDA_REDUCE_ROWS 6
+#endif
 constexpr int kChunk = 4096;         // entries of one reduction block
 constexpr int kEntryCellShift = 24;  // entry.x = row | cell << 24 (rows < 2^24, cells < 2^8)
 static_assert(kTileCells * kTileCells <= (1 << (32 - kEntryCellShift)), "cell index must fit above the row");
@@ -1371,7 +1374,8 @@ msda_tile_reduce_kernel(const __grid_constant__ Params p, const T *__restrict__ 
                 for (int e = 0; e < VEC; ++e) acc[i][k][e] = 0.0f;
         }
     };
-    constexpr int U = NCH >= 8 ? 1 : 8 / NCH;  // grad_output rows in flight (32 registers of them)
+    // grad_output rows in flight a group (one chunk a lane: MSDA_REDUCE_ROWS; wider rows: 32 registers of them)
+    constexpr int U = NCH >= 8 ? 1 : (NCH == 1 ? MSDA_REDUCE_ROWS : 8 / NCH);
     for (int s0 = s_beg; s0 < s_end; s0 += U) {
         int ei[U];
         float gv[U][NCH][VEC];
