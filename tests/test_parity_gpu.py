@@ -399,3 +399,14 @@ def test_whole_row_scatter_matrix(dtype, pad, align, vl, ll, aggregate, N_p, mon
     check_workload(_whole_rows(dtype, vl, ll, align, pad, seed=17 + N_p, N_p=N_p),
                    flag_sets=[(True, True, True), (True, True, False), (True, False, True), (False, True, True)],
                    check_forward=N_p == 4)
+
+
+@pytest.mark.parametrize("aggregate", ["1", "0"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_grad_value_only_row_kernel(dtype, aggregate, monkeypatch):
+    """grad_value alone on a problem too sparse for the tile-sorted path but
+    with whole rows (decoder-style queries, 2 x 2000 x 8 rows): the row
+    kernel's grad_value-only instantiation, aggregated and plain."""
+    monkeypatch.setenv("MSDA_BWD_AGGREGATE", aggregate)
+    w = gen.WORKLOADS["decoder"].with_(N_q=2000, dtype=dtype, seed=27)
+    check_workload(w, flag_sets=[(True, False, False), (True, True, True)], check_forward=False)

@@ -62,6 +62,7 @@ def _outs(t, flags):
 @pytest.mark.parametrize("name,dtype,flags", [
     ("decoder-1img-bf16", "bf16", (1, 1, 1)),
     ("decoder-1img-bf16", "bf16", (1, 0, 0)),
+    ("encoder-1img-bf16", "bf16", (1, 0, 0)),
     ("tiny-bf16", "bf16", (1, 1, 1)),
     ("tiny-f32", "f32", (1, 1, 1)),
 ])
@@ -69,6 +70,10 @@ def test_noalloc_matches_backward_twice(lib, name, dtype, flags):
     if name.startswith("decoder"):
         # one image of the Deformable-DETR pyramid: a 5.7M-element accumulator
         w = gen.WORKLOADS["decoder"].with_(B=1, dtype=dtype, seed=21)
+    elif name.startswith("encoder"):
+        # one image, one query per pixel: whole rows, grad_value by the row kernel
+        # (msda_backward takes the tile-sorted path for this grad_value-only call)
+        w = gen.WORKLOADS["encoder32"].with_(B=1, dtype=dtype, seed=23)
     else:
         w = gen.WORKLOADS["tiny"].with_(dtype=dtype, seed=22)
     assert 4 * w.B * w.L * w.N_h * w.C_h <= SCRATCH_BYTES
