@@ -441,6 +441,9 @@ __device__ __forceinline__ float2 row_softmax_stats(const float *attn, int64_t a
 }
 
 // ---------------------------------------------------------------- forward
+#ifndef MSDA_FWD_INFLIGHT
+#define MSDA_FWD_INFLIGHT 2
+#endif
 #ifndef MSDA_FWD_MIN_BLOCKS
 #define MSDA_FWD_MIN_BLOCKS 4
 #endif
@@ -598,7 +601,8 @@ msda_forward_kernel(const __grid_constant__ Params p, const T *__restrict__ valu
             if constexpr (REC) __syncwarp(gmask);
             // consume phase: the group's samples in order, corners of two in flight
             const int ns = FULL ? G : min(G, NLP - j0);  // (FULL: every batch has G samples)
-            constexpr int S2 = (G >= 2 && NCH * VEC <= 4) ? 2 : 1;  // two samples in flight for one chunk a lane
+            // samples in flight for one chunk a lane (MSDA_FWD_INFLIGHT, a divisor of G)
+            constexpr int S2 = (G >= 2 && NCH * VEC <= 4) ? (MSDA_FWD_INFLIGHT < G ? MSDA_FWD_INFLIGHT : G) : 1;
 #pragma unroll
             for (int s = 0; s < G; s += S2) {
                 if constexpr (NCH > 4) {  // wide rows: the same arithmetic, two chunks' corners at a time
