@@ -258,6 +258,15 @@ __device__ __forceinline__ void stl(float *base, int64_t i, float v, int dt) {
     else if (dt == 1) reinterpret_cast<__nv_bfloat16 *>(base)[i] = __float2bfloat16_rn(v);
     else reinterpret_cast<__half *>(base)[i] = __float2half_rn(v);
 }
+// The store counterpart of ld_uv.
+__device__ __forceinline__ void st_uv(float *base, int64_t i, int sXY, int dt, bool pair, float x, float y) {
+    if (pair) {
+        *reinterpret_cast<float2 *>(base + i) = make_float2(x, y);
+    } else {
+        stl(base, i, x, dt);
+        stl(base, i + sXY, y, dt);
+    }
+}
 
 // ---------------------------------------------------------------- geometry
 struct Row {
@@ -922,6 +931,7 @@ msda_backward_kernel(const __grid_constant__ Params p, const T *__restrict__ gra
     const int mypos = rec_pos<G>(grp, r);
     const int sP = p.v_sP, sJ = p.l_sJ, sXY = p.l_sXY, NLP = p.NLP;
     const bool lpair = sXY == 1 && sJ == 2 && p.loc_dt == 0 && !(reinterpret_cast<uintptr_t>(loc) & 7u);
+    const bool gpair = sXY == 1 && sJ == 2 && p.loc_dt == 0 && !(reinterpret_cast<uintptr_t>(grad_loc) & 7u);
     int nk = 0;  // chunks this lane owns: k*G + r < chunks (FULL: all NCH)
 #pragma unroll
     for (int k = 0; k < NCH; ++k) nk += (FULL || k * G + r < p.chunks);
@@ -1109,8 +1119,9 @@ msda_backward_kernel(const __grid_constant__ Params p, const T *__restrict__ gra
                     if (want_ga) stl(grad_attn, ao + j, ga, p.loc_dt);  // (logits: <g, S_j>, made d/dlogit below)
                     if (soft) sAg = fmaf(A, ga, sAg);
                     if (want_gl) {
-                        stl(grad_loc, lrow + j * sJ, A * tx * (lt.sx[l] * c.kx), p.loc_dt);
-                        stl(grad_loc, lrow + j * sJ + sXY, A * ty * (lt.sy[l] * c.ky), p.loc_dt);
+                        const float2 sxy = *reinterpret_cast<const float2 *>(&lt.geo[l]);
+                        st_uv(grad_loc, lrow + j * sJ, sXY, p.loc_dt, gpair, A * tx * (sxy.x * c.kx),
+                              A * ty * (sxy.y * c.ky));
                     }
                 }
             }
