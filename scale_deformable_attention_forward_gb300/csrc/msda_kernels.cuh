@@ -798,33 +798,40 @@ __device__ __forceinline__ int agg_scatter(AggTable &tab, int4 o4, float4 w4, in
     const unsigned gmask = 0xffu << gbase;
     const int key4[4] = {o4.x, o4.y, o4.z, o4.w};
     const float wt4[4] = {w4.x, w4.y, w4.z, w4.w};
-    // insert the four corners: the table sums each row's weights per pixel
+    // insert the four corners: the table sums each row's weights per pixel;
+    // the four first probes go out back to back, collisions probe on after
     int nrec = 0, ncon = 0;
     unsigned ovf = 0;  // corners of this lane that found no slot
+    bool want[4];
+    unsigned sl[4];
+    int old[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        const bool want = wt4[i] != 0.0f;
+        want[i] = wt4[i] != 0.0f;
+        sl[i] = agg_hash(key4[i]);
+        old[i] = want[i] ? atomicCAS(&tab.key[sl[i]], -1, key4[i]) : -1;
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
         bool fresh = false;
-        unsigned s = 0;
-        if (want) {
-            bool placed = false;
-            s = agg_hash(key4[i]);
-            for (int t = 0; t < kAggProbes; ++t) {
-                const int old = atomicCAS(&tab.key[s], -1, key4[i]);
-                if (old == -1 || old == key4[i]) {
-                    placed = true;
-                    fresh = old == -1;
-                    break;
-                }
+        if (want[i]) {
+            bool placed = old[i] == -1 || old[i] == key4[i];
+            fresh = old[i] == -1;
+            unsigned s = sl[i];
+            for (int t = 1; t < kAggProbes && !placed; ++t) {
                 s = (s + 1) & (kAggSlots - 1);
+                const int o2 = atomicCAS(&tab.key[s], -1, key4[i]);
+                placed = o2 == -1 || o2 == key4[i];
+                fresh = o2 == -1;
             }
+            sl[i] = s;
             if (placed) atomicAdd(reinterpret_cast<float *>(&tab.w[s]) + grp, wt4[i]);
             else ovf |= 1u << i;
         }
         const unsigned nm = __ballot_sync(0xffffffffu, fresh);
-        if (fresh) tab.list[nrec + __popc(nm & below)] = (unsigned char)s;
+        if (fresh) tab.list[nrec + __popc(nm & below)] = (unsigned char)sl[i];
         nrec += __popc(nm);
-        ncon += __popc(__ballot_sync(0xffffffffu, want));
+        ncon += __popc(__ballot_sync(0xffffffffu, want[i]));
     }
     // contributions that found no slot: their row's group adds them directly
 #pragma unroll
