@@ -71,6 +71,24 @@ def compulsory_bytes(w: gen.Workload):
     return fwd, bwd
 
 
+def gather_roofline(w: gen.Workload, fwd_ms: float, n_sm: int, sm_mhz) -> dict:
+    """The forward against its L1 ceiling: samples x 4 corner rows x the
+    128-byte lines of one row (C_h values of value's dtype), one line per
+    L1 data-pipe wavefront and one wavefront per SM per cycle, at the median
+    SM clock sampled during the timed region (the GPU's maximum clock when no
+    sample was taken)."""
+    ev = 2 if w.dtype == "bf16" else 4
+    lines = w.samples * 4 * -(-(w.C_h * ev) // 128)
+    mhz = float(sm_mhz) if sm_mhz else 2070.0
+    achieved = lines / (fwd_ms * 1e-3) / 1e9
+    peak = n_sm * mhz * 1e-3
+    return {"what": "forward corner-row reads (samples x 4 corners x 128-byte lines a row) / forward time, against "
+                    "one L1 data-pipe wavefront per SM per cycle",
+            "achieved": round(achieved, 2), "peak": round(peak, 2), "unit": "Glines/s",
+            "frac": round(achieved / peak, 4),
+            "peak_source": f"{n_sm} SMs x {mhz:.0f} MHz" + ("" if sm_mhz else " (maximum clock: no clock sample)")}
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     for f in sorted(os.listdir(CSRC)):
@@ -726,6 +744,10 @@ def run_ours(args, w: gen.Workload):
             "bwd_ms": round(plain_bwd_ms, 6), "aggregated_bwd_ms": round(bwd_mean, 6),
             "aggregated_speedup": round(plain_bwd_ms / bwd_mean, 4) if bwd_mean > 0 else None,
             "loc_attn_grads_bit_identical": plain_same},
+        # The forward's own bound: each sample reads four corner rows, and the L1 data pipe
+        # serves one line of them (one wavefront) per SM per cycle, whoever reads it.
+        "roofline_gather": gather_roofline(w, fwd_mean, torch.cuda.get_device_properties(dev).multi_processor_count,
+                                           clocks.get("sm_mhz")),
         "roofline_step": {
             "what": "forward + backward compulsory bytes / step time",
             "achieved": round((fwd_b + bwd_b) / (step_ms * 1e-3) / 1e9, 1), "peak": peak, "unit": "GB/s",
