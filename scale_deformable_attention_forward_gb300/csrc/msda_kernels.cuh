@@ -586,7 +586,7 @@ msda_forward_kernel(const __grid_constant__ Params p, const T *__restrict__ valu
         float nu = 0.0f, nv = 0.0f, nA = 0.0f;
         if constexpr (LA) {
             const int j = part * G + r;
-            if (FULL || j < NLP) {  // (FULL: every batch is whole, and part * G < NLP)
+            if (j < NLP) {
                 ld_uv(loc, lo + j * sJ, sXY, ldt, lpair, nu, nv);
                 nA = ldl(attn, ao + j, ldt);
             }
@@ -603,7 +603,7 @@ msda_forward_kernel(const __grid_constant__ Params p, const T *__restrict__ valu
                     nA = ldl(attn, ao + jn, ldt);
                 }
             }
-            if (FULL || j < NLP) {
+            if (FULL || j < NLP) {  // (FULL: every batch the loop reaches is whole)
                 const float u = LA ? cu : ldl(loc, lo + j * sJ, ldt), v = LA ? cv : ldl(loc, lo + j * sJ + sXY, ldt);
                 float A = LA ? cA : ldl(attn, ao + j, ldt);
                 if (logits) A = expf(A - sm.x) * sm.y;

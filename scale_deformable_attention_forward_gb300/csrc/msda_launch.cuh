@@ -58,7 +58,7 @@ cudaError_t fwd_split(const Params &p, const T *value, const float *loc, const f
                       cudaStream_t stream) {
     // full rows (no partial batch, no masked lane): the guard-free instantiation
     if constexpr (MSDA_FWD_FULL && !GEN) {
-        if (p.NLP % GG == 0 && p.chunks == GG * NN)
+        if (p.NLP > 0 && p.NLP % GG == 0 && p.chunks == GG * NN)
             return fwd_launch<T, V, GG, NN, PAD, GEN, true, true>(p, value, loc, attn, out, stream);
     }
     return fwd_launch<T, V, GG, NN, PAD, GEN, true>(p, value, loc, attn, out, stream);
@@ -119,7 +119,7 @@ template <typename T, int V, int GG, int NN, int PAD, int FL, bool SPLIT, bool A
 cudaError_t bwd_launch_agg(const Params &q, const T *grad_out, const T *value, const float *loc, const float *attn,
                            const BwdBuffers &bb, cudaStream_t stream) {
     if constexpr (MSDA_BWD_FULL && PAD >= 0 && !SPLIT && (AGG || FL == (kGradLoc | kGradAttn))) {
-        if (q.NLP % GG == 0 && q.chunks == GG * NN)
+        if (q.NLP > 0 && q.NLP % GG == 0 && q.chunks == GG * NN)
             return bwd_launch_full<T, V, GG, NN, PAD, FL, SPLIT, AGG, true>(q, grad_out, value, loc, attn, bb, stream);
     }
     return bwd_launch_full<T, V, GG, NN, PAD, FL, SPLIT, AGG, false>(q, grad_out, value, loc, attn, bb, stream);
